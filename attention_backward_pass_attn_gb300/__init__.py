@@ -1,0 +1,24 @@
+"""GB300-native exact-attention forward and fused backward.
+
+The CUDA kernels live in ``csrc/`` and are compiled for sm_103a into the
+in-tree shared library ``libattn_gb300.so``, whose C ABI is declared in
+``include/attn.h``.  ``binding`` wraps that ABI with ctypes; PyTorch only
+provides device memory and streams.  Importing this package does not load the
+library; the first call into ``binding`` does, and raises if it is missing.
+"""
+
+from .inputs import WORKLOADS, WORKLOAD_ORDER, Workload, make_inputs  # noqa: F401
+
+_BINDING_NAMES = (
+    "attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
+    "attn_bwd_dq_convert", "attn_bwd_workspace_size", "attn_last_device_error",
+    "AttnError", "load_library",
+)
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        from . import binding
+
+        return getattr(binding, name)
+    raise AttributeError(name)

@@ -1,0 +1,301 @@
+"""Pins that tie the fp64 oracle to facts other than itself.
+
+Each ``pin_*`` function takes a loaded oracle library (so the same checks can
+be run against deliberately broken copies of the oracle) and raises
+AssertionError when the oracle disagrees with:
+
+* central finite differences of its own forward (the gradient must be the
+  derivative of the loss <dO, O>),
+* closed forms (one key; zero queries; identical keys; two keys),
+* invariants of softmax attention (rows of P sum to one, rows of dS sum to
+  zero, shifting every key by one vector, permuting keys),
+* PyTorch's own fp64 CPU attention and autograd (an independent library
+  routine, used as a cross-check only),
+* a pure-Python brute force over the full N x N matrices for N <= 8.
+
+The method is exact attention as named by "Training Transformers and Hybrid
+models on AMD Instinct MI300X Accelerators", section "Flash Attention"; the
+pages print no worked example, so every pin is mathematical.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+
+
+def _rand(rng, shape, std=1.0):
+    return rng.standard_normal(shape) * std
+
+
+def _fb(lib, q, k, v, do, causal, scale):
+    return oracle.attention_forward_backward(q, k, v, do, causal, scale, lib=lib)
+
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, "%s: shape %s vs %s" % (what, a.shape, b.shape)
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    ref = max(np.max(np.abs(b)) if b.size else 0.0, 1e-300)
+    assert np.all(np.isfinite(a)), "%s: non-finite values" % what
+    assert err <= rtol * ref + atol, "%s: max|err| %.3e > %.1e * %.3e + %.1e" % (
+        what, err, rtol, ref, atol)
+
+
+# --------------------------------------------------------------------------
+# Finite differences: the backward is the derivative of the forward.
+# --------------------------------------------------------------------------
+def pin_finite_differences(lib):
+    rng = np.random.default_rng(11)
+    for causal in (False, True):
+        for (N, d) in ((1, 2), (3, 2), (6, 4), (8, 3)):
+            q, k, v, do = (_rand(rng, (1, 2, N, d)) for _ in range(4))
+            scale = 0.7
+            out = _fb(lib, q, k, v, do, causal, scale)
+
+            def loss(q_, k_, v_):
+                o, _ = oracle.attention_forward(q_, k_, v_, causal, scale, lib=lib)
+                return float(np.sum(do * o))
+
+            h = 1e-6
+            for name, x, g in (("dQ", q, out["dQ"]), ("dK", k, out["dK"]),
+                               ("dV", v, out["dV"])):
+                num = np.zeros_like(x)
+                for idx in np.ndindex(x.shape):
+                    xp = x.copy(); xp[idx] += h
+                    xm = x.copy(); xm[idx] -= h
+                    args_p = [q, k, v]; args_m = [q, k, v]
+                    pos = {"dQ": 0, "dK": 1, "dV": 2}[name]
+                    args_p[pos] = xp; args_m[pos] = xm
+                    num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+                _close(g, num, rtol=1e-6, atol=1e-8,
+                       what="finite differences %s N=%d d=%d causal=%s" % (name, N, d, causal))
+
+
+# --------------------------------------------------------------------------
+# Closed forms.
+# --------------------------------------------------------------------------
+def pin_single_key(lib):
+    """N = 1: softmax over one key is 1, so O = V, L = s<q,k>, dV = dO, dQ = dK = 0."""
+    rng = np.random.default_rng(12)
+    for causal in (False, True):
+        q, k, v, do = (_rand(rng, (2, 3, 1, 5)) for _ in range(4))
+        s = 0.3
+        out = _fb(lib, q, k, v, do, causal, s)
+        _close(out["O"], v, 1e-15, what="N=1 O")
+        _close(out["L"], s * np.sum(q * k, axis=-1), 1e-14, 1e-15, what="N=1 L")
+        _close(out["dV"], do, 1e-15, what="N=1 dV")
+        _close(out["dQ"], np.zeros_like(q), 0.0, 1e-15, what="N=1 dQ")
+        _close(out["dK"], np.zeros_like(k), 0.0, 1e-15, what="N=1 dK")
+
+
+def pin_zero_queries(lib):
+    """Q = 0: every unmasked score is 0, so P is uniform over the unmasked keys.
+
+    Non-causal: O_i = mean_j v_j and L_i = ln N.  Causal: O_i is the mean of
+    v_0..v_i and L_i = ln(i + 1).
+    """
+    rng = np.random.default_rng(13)
+    N, d = 37, 6
+    q = np.zeros((1, 2, N, d))
+    k, v, do = (_rand(rng, (1, 2, N, d)) for _ in range(3))
+    out = _fb(lib, q, k, v, do, False, 0.4)
+    _close(out["O"], np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape), 1e-13,
+           what="Q=0 O")
+    _close(out["L"], np.full((1, 2, N), math.log(N)), 1e-14, what="Q=0 L")
+    out = _fb(lib, q, k, v, do, True, 0.4)
+    prefix = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    _close(out["O"], prefix, 1e-13, what="Q=0 causal O")
+    _close(out["L"], np.broadcast_to(np.log(np.arange(1, N + 1)), (1, 2, N)), 1e-14,
+           what="Q=0 causal L")
+
+
+def pin_identical_keys(lib):
+    """All keys equal (non-causal): P is uniform and dS rows sum to zero, so
+    O = mean(V), dQ = 0, and dV_j = mean_i-sum of dO / N for every j."""
+    rng = np.random.default_rng(14)
+    N, d = 19, 4
+    q, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(3))
+    k = np.broadcast_to(_rand(rng, (1, 1, 1, d)), (1, 1, N, d)).copy()
+    out = _fb(lib, q, k, v, do, False, 0.9)
+    _close(out["O"], np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape), 1e-13,
+           what="equal keys O")
+    _close(out["dQ"], np.zeros_like(q), 0.0, 1e-13, what="equal keys dQ")
+    _close(out["dV"], np.broadcast_to(do.sum(axis=2, keepdims=True) / N, do.shape), 1e-13,
+           what="equal keys dV")
+
+
+def pin_two_keys_logistic(lib):
+    """Two keys, d = 1, non-causal: P_i0 = sigmoid(s q_i (k_0 - k_1)).
+
+    Then O_i = v_1 + sigmoid(a_i) (v_0 - v_1), and with a_i = s q_i (k_0 - k_1),
+    dQ_i = s (k_0 - k_1) sigma'(a_i) (v_0 - v_1) dO_i.
+    """
+    q = np.array([0.5, -1.25, 2.0]).reshape(1, 1, 3, 1)
+    k = np.array([0.75, -0.5, 0.0]).reshape(1, 1, 3, 1)
+    # only the first two keys exist: N must match, so build N=2 queries twice
+    for i in range(3):
+        qi = q[:, :, i:i + 1, :].repeat(2, axis=2)
+        kk = k[:, :, :2, :]
+        v = np.array([3.0, -1.0]).reshape(1, 1, 2, 1)
+        do = np.array([0.25, 0.0]).reshape(1, 1, 2, 1)
+        s = 1.5
+        out = _fb(lib, qi, kk, v, do, False, s)
+        a = s * q[0, 0, i, 0] * (k[0, 0, 0, 0] - k[0, 0, 1, 0])
+        sig = 1.0 / (1.0 + math.exp(-a))
+        o_expect = v[0, 0, 1, 0] + sig * (v[0, 0, 0, 0] - v[0, 0, 1, 0])
+        assert abs(out["O"][0, 0, 0, 0] - o_expect) <= 1e-14, "two-key O"
+        dq_expect = (s * (k[0, 0, 0, 0] - k[0, 0, 1, 0]) * sig * (1 - sig)
+                     * (v[0, 0, 0, 0] - v[0, 0, 1, 0]) * do[0, 0, 0, 0])
+        assert abs(out["dQ"][0, 0, 0, 0] - dq_expect) <= 1e-14, "two-key dQ"
+        lse = max(s * q[0, 0, i, 0] * k[0, 0, 0, 0], s * q[0, 0, i, 0] * k[0, 0, 1, 0])
+        lse += math.log(math.exp(s * q[0, 0, i, 0] * k[0, 0, 0, 0] - lse)
+                        + math.exp(s * q[0, 0, i, 0] * k[0, 0, 1, 0] - lse))
+        assert abs(out["L"][0, 0, 0] - lse) <= 1e-14, "two-key L"
+
+
+# --------------------------------------------------------------------------
+# Invariants.
+# --------------------------------------------------------------------------
+def pin_invariants(lib):
+    """Rows of P sum to one and rows of dS sum to zero, seen through outputs.
+
+    * sum_j dV_j = sum_i (sum_j P_ij) dO_i = sum_i dO_i.
+    * sum_j dK_j = s sum_i q_i sum_j dS_ij = 0.
+    * adding one vector c to every key leaves O, dQ, dK, dV unchanged and moves
+      L_i by s <q_i, c> (each score row moves by a constant).
+    * O_i is a convex combination of the value rows it can see.
+    * scaling V scales O and leaves dV unchanged (dV = P^T dO).
+    """
+    rng = np.random.default_rng(15)
+    for causal in (False, True):
+        B, H, N, d = 2, 2, 45, 7
+        q, k, v, do = (_rand(rng, (B, H, N, d)) for _ in range(4))
+        s = 0.45
+        out = _fb(lib, q, k, v, do, causal, s)
+        _close(out["dV"].sum(axis=2), do.sum(axis=2), 1e-12, what="sum dV = sum dO")
+        _close(out["dK"].sum(axis=2), np.zeros((B, H, d)), 0.0,
+               1e-12 * np.abs(out["dK"]).max(), what="sum dK = 0")
+        c = _rand(rng, (1, 1, 1, d))
+        out2 = _fb(lib, q, k + c, v, do, causal, s)
+        for name in ("O", "dQ", "dK", "dV"):
+            _close(out2[name], out[name], 1e-11, what="key shift %s" % name)
+        _close(out2["L"], out["L"] + s * np.sum(q * c, axis=-1), 1e-12,
+               what="key shift L")
+        if causal:
+            lo = np.minimum.accumulate(v, axis=2)
+            hi = np.maximum.accumulate(v, axis=2)
+        else:
+            lo = np.broadcast_to(v.min(axis=2, keepdims=True), v.shape)
+            hi = np.broadcast_to(v.max(axis=2, keepdims=True), v.shape)
+        assert np.all(out["O"] >= lo - 1e-12) and np.all(out["O"] <= hi + 1e-12), "convexity"
+        out3 = _fb(lib, q, k, 2.5 * v, do, causal, s)
+        _close(out3["O"], 2.5 * out["O"], 1e-13, what="V scaling O")
+        _close(out3["dV"], out["dV"], 1e-13, what="V scaling dV")
+        _close(out["D"], np.sum(do * out["O"], axis=-1), 1e-13, what="D = rowsum(dO*O)")
+
+
+def pin_permutation(lib):
+    """Non-causal attention is equivariant in the queries and invariant to a
+    joint permutation of the keys and values."""
+    rng = np.random.default_rng(16)
+    N, d = 23, 5
+    q, k, v, do = (_rand(rng, (1, 2, N, d)) for _ in range(4))
+    out = _fb(lib, q, k, v, do, False, 0.6)
+    pk = rng.permutation(N)
+    pq = rng.permutation(N)
+    out2 = _fb(lib, q[:, :, pq], k[:, :, pk], v[:, :, pk], do[:, :, pq], False, 0.6)
+    for name in ("O", "dQ"):
+        _close(out2[name], out[name][:, :, pq], 1e-12, what="perm %s" % name)
+    _close(out2["L"], out["L"][:, :, pq], 1e-12, what="perm L")
+    for name in ("dK", "dV"):
+        _close(out2[name], out[name][:, :, pk], 1e-12, what="perm %s" % name)
+
+
+# --------------------------------------------------------------------------
+# Brute force over the full matrices, pure Python loops, tiny N.
+# --------------------------------------------------------------------------
+def _brute(q, k, v, do, causal, s):
+    N, d = len(q), len(q[0])
+    S = [[(s * sum(q[i][c] * k[j][c] for c in range(d)) if (not causal or j <= i)
+           else -math.inf) for j in range(N)] for i in range(N)]
+    L = []
+    for i in range(N):
+        m = max(S[i])
+        L.append(m + math.log(sum(math.exp(x - m) for x in S[i])))
+    P = [[math.exp(S[i][j] - L[i]) for j in range(N)] for i in range(N)]
+    O = [[sum(P[i][j] * v[j][c] for j in range(N)) for c in range(d)] for i in range(N)]
+    dP = [[sum(do[i][c] * v[j][c] for c in range(d)) for j in range(N)] for i in range(N)]
+    D = [sum(do[i][c] * O[i][c] for c in range(d)) for i in range(N)]
+    dS = [[P[i][j] * (dP[i][j] - D[i]) for j in range(N)] for i in range(N)]
+    dQ = [[s * sum(dS[i][j] * k[j][c] for j in range(N)) for c in range(d)] for i in range(N)]
+    dK = [[s * sum(dS[i][j] * q[i][c] for i in range(N)) for c in range(d)] for j in range(N)]
+    dV = [[sum(P[i][j] * do[i][c] for i in range(N)) for c in range(d)] for j in range(N)]
+    rowsum_P = [sum(P[i]) for i in range(N)]
+    rowsum_dS = [sum(dS[i]) for i in range(N)]
+    return dict(O=O, L=L, D=D, dQ=dQ, dK=dK, dV=dV, rowsum_P=rowsum_P, rowsum_dS=rowsum_dS)
+
+
+def pin_brute_force(lib):
+    rng = np.random.default_rng(17)
+    for causal in (False, True):
+        for N, d in ((2, 1), (5, 3), (8, 4)):
+            q, k, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(4))
+            s = 0.8
+            out = _fb(lib, q, k, v, do, causal, s)
+            ref = _brute(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(),
+                         do[0, 0].tolist(), causal, s)
+            _close(ref["rowsum_P"], np.ones(N), 1e-14, what="brute rowsum P")
+            assert max(abs(x) for x in ref["rowsum_dS"]) < 1e-12, "brute rowsum dS"
+            for name in ("O", "dQ", "dK", "dV"):
+                _close(out[name][0, 0], np.array(ref[name]), 1e-12,
+                       what="brute %s N=%d causal=%s" % (name, N, causal))
+            for name in ("L", "D"):
+                _close(out[name][0, 0], np.array(ref[name]), 1e-12,
+                       what="brute %s" % name)
+
+
+# --------------------------------------------------------------------------
+# Independent library cross-check: PyTorch fp64 CPU attention + autograd.
+# --------------------------------------------------------------------------
+def pin_torch_fp64(lib):
+    import torch
+
+    rng = np.random.default_rng(18)
+    for causal in (False, True):
+        for (B, H, N, d) in ((1, 2, 64, 16), (2, 1, 131, 8), (1, 1, 300, 32)):
+            q, k, v, do = (_rand(rng, (B, H, N, d)) for _ in range(4))
+            s = 1.0 / math.sqrt(d)
+            out = _fb(lib, q, k, v, do, causal, s)
+            tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True)
+                          for x in (q, k, v))
+            to = torch.nn.functional.scaled_dot_product_attention(
+                tq, tk, tv, is_causal=causal, scale=s)
+            to.backward(torch.tensor(do, dtype=torch.float64))
+            scores = (tq.detach() @ tk.detach().transpose(-1, -2)) * s
+            if causal:
+                mask = torch.ones(N, N, dtype=torch.bool).triu(1)
+                scores = scores.masked_fill(mask, float("-inf"))
+            tl = torch.logsumexp(scores, dim=-1)
+            _close(out["O"], to.detach().numpy(), 1e-11, what="torch O")
+            _close(out["L"], tl.numpy(), 1e-12, what="torch L")
+            _close(out["dQ"], tq.grad.numpy(), 1e-10, what="torch dQ")
+            _close(out["dK"], tk.grad.numpy(), 1e-10, what="torch dK")
+            _close(out["dV"], tv.grad.numpy(), 1e-10, what="torch dV")
+
+
+ALL_PINS = [
+    pin_finite_differences,
+    pin_single_key,
+    pin_zero_queries,
+    pin_identical_keys,
+    pin_two_keys_logistic,
+    pin_invariants,
+    pin_permutation,
+    pin_brute_force,
+    pin_torch_fp64,
+]
