@@ -1,0 +1,215 @@
+"""ctypes binding of the C ABI in ``include/attn.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libattn_gb300.so``.  PyTorch supplies device memory (outputs and
+the backward's workspace are allocated here with ``torch.empty`` unless the
+caller passes them) and the current CUDA stream.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_WORKSPACE = 5
+ATTN_ERR_DEVICE = 6
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__("%s failed: %s (status %d)" % (fn, text, status))
+        self.status = status
+
+
+def load_library(path: str | None = None):
+    """Load ``libattn_gb300.so`` (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                "CUDA library %s is not built; run __graft_entry__.build() (needs nvcc). "
+                "There is no CPU fallback." % p)
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        sig = {
+            "attn_fwd": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]),
+            "attn_bwd_workspace_size": (sz, [i, i, i, i]),
+            "attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
+            "attn_bwd_preprocess": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
+            "attn_bwd_main": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
+            "attn_bwd_dq_convert": (i, [vp, i, i, i, i, f, vp, sz, vp]),
+            "attn_last_device_error": (i, [vp]),
+            "attn_device_error_word": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
+            "attn_watchdog_selftest": (i, [ctypes.c_uint64, vp]),
+            "attn_status_string": (ctypes.c_char_p, [i]),
+            "attn_version": (i, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != ATTN_OK:
+        raise AttnError(fn, status, status_string(status))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _shape4(t: torch.Tensor, name: str):
+    if t.dim() != 4:
+        raise ValueError("%s must be [B, H, N, d], got %s" % (name, tuple(t.shape)))
+    return tuple(t.shape)
+
+
+def _check_tensor(t: torch.Tensor, name: str, shape, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _default_scale(d: int, scale):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, H, N, d))
+
+
+def alloc_workspace(B: int, H: int, N: int, d: int, device) -> torch.Tensor:
+    """A uint8 device buffer of the size attn_bwd needs (torch allocations are
+    256-byte aligned)."""
+    n = max(attn_bwd_workspace_size(B, H, N, d), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None):
+    """O = softmax(scale q k^T [+ causal mask]) v and the row log-sum-exp L.
+
+    q, k, v: bf16 CUDA tensors [B, H, N, d] (d = 64 or 128), contiguous.
+    Returns (O bf16 [B, H, N, d], L fp32 [B, H, N]).
+    """
+    B, H, N, d = _shape4(q, "q")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, (B, H, N, d))
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor(out, "out", (B, H, N, d))
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    st = load_library().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, int(bool(causal)),
+                                 _default_scale(d, scale), _stream(stream))
+    _check("attn_fwd", st)
+    return out, lse
+
+
+def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """dQ, dK, dV of exact attention (the fused backward, three kernels).
+
+    o, lse: the forward's outputs; do: the upstream gradient of o.
+    Returns (dQ, dK, dV), bf16 [B, H, N, d].
+    """
+    B, H, N, d = _shape4(q, "q")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _check_tensor(t, n, (B, H, N, d))
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check_tensor(t, n, (B, H, N, d))
+    if workspace is None:
+        workspace = alloc_workspace(B, H, N, d, q.device)
+    st = load_library().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), B, H, N, d, int(bool(causal)),
+                                 _default_scale(d, scale), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("attn_bwd", st)
+    return dq, dk, dv
+
+
+def attn_bwd_preprocess(o, do, lse, workspace, stream=None):
+    B, H, N, d = _shape4(o, "o")
+    st = load_library().attn_bwd_preprocess(o.data_ptr(), do.data_ptr(), lse.data_ptr(), B, H, N,
+                                            d, workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream(stream))
+    _check("attn_bwd_preprocess", st)
+
+
+def attn_bwd_main(q, k, v, do, dk, dv, causal: bool, workspace, scale=None, stream=None):
+    B, H, N, d = _shape4(q, "q")
+    st = load_library().attn_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                      dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                      int(bool(causal)), _default_scale(d, scale),
+                                      workspace.data_ptr(),
+                                      workspace.numel() * workspace.element_size(),
+                                      _stream(stream))
+    _check("attn_bwd_main", st)
+
+
+def attn_bwd_dq_convert(dq, workspace, scale=None, stream=None):
+    B, H, N, d = _shape4(dq, "dq")
+    st = load_library().attn_bwd_dq_convert(dq.data_ptr(), B, H, N, d, _default_scale(d, scale),
+                                            workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream(stream))
+    _check("attn_bwd_dq_convert", st)
+
+
+def attn_last_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load_library().attn_last_device_error(_stream(stream)))
+
+
+def attn_device_error_word(stream=None):
+    w = ctypes.c_int(0)
+    st = load_library().attn_device_error_word(_stream(stream), ctypes.byref(w))
+    return int(st), int(w.value)
+
+
+def attn_watchdog_selftest(limit_ns: int, stream=None) -> int:
+    return int(load_library().attn_watchdog_selftest(int(limit_ns), _stream(stream)))

@@ -1,0 +1,262 @@
+// attn_api.cu -- the library's C ABI (declared in include/attn.h): argument
+// validation, TMA tensor-map encoding, workspace carve-up, the per-device
+// error word, and the calls into the kernel launchers.
+
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+// The device error word the kernels report failures into.  Host code never
+// dereferences the symbol: it asks the runtime for its device address.
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int* error_word_ptr() {
+  static std::mutex mu;
+  static int* ptrs[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Validate sizes and flags; fill `s`.  Returns ATTN_OK, or an error, or
+// (through *empty) that the problem has no rows.
+int make_shape(int B, int H, int N, int d, int causal, Shape* s, bool* empty) {
+  if (B < 0 || H < 0 || N < 0 || d < 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  *empty = (B == 0 || H == 0 || N == 0);
+  if (*empty) return ATTN_OK;
+  const long long BH = (long long)B * H;
+  const long long n_tiles = (N + 127LL) / 128;
+  // Keep every row index (and the grid size) inside 31 bits.
+  if (BH > INT_MAX || BH * n_tiles * 128 > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  s->BH = int(BH);
+  s->N = N;
+  s->d = d;
+  s->causal = causal;
+  s->n_tiles = int(n_tiles);
+  s->Npad = int(n_tiles * 128);
+  return ATTN_OK;
+}
+
+bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+int check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+int check_workspace(const void* ws, size_t bytes, const Shape& s) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return ATTN_ERR_WORKSPACE;
+  if (bytes < workspace_bytes(s)) return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+size_t workspace_bytes(const Shape& s) {
+  const size_t vec = round256(sizeof(float) * size_t(s.BH) * s.Npad);
+  const size_t acc = round256(sizeof(float) * size_t(s.BH) * s.Npad * s.d);
+  return 2 * vec + acc;
+}
+
+Workspace carve_workspace(void* base, const Shape& s) {
+  const size_t vec = round256(sizeof(float) * size_t(s.BH) * s.Npad);
+  char* p = static_cast<char*>(base);
+  Workspace w;
+  w.L2 = reinterpret_cast<float*>(p);
+  w.D = reinterpret_cast<float*>(p + vec);
+  w.acc = reinterpret_cast<float*>(p + 2 * vec);
+  return w;
+}
+
+int make_tile_map(CUtensorMap* map, const void* ptr, const Shape& s) {
+  auto encode = encode_fn();
+  if (!encode) return -1;
+  const cuuint64_t dims[3] = {cuuint64_t(s.d), cuuint64_t(s.N), cuuint64_t(s.BH)};
+  const cuuint64_t strides[2] = {cuuint64_t(s.d) * 2, cuuint64_t(s.N) * s.d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128)";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ATTN_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+  Shape s;
+  bool empty = false;
+  if (make_shape(B, H, N, d, 0, &s, &empty) != ATTN_OK || empty) return 0;
+  return workspace_bytes(s);
+}
+
+int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N,
+             int d, int causal, float scale, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q, K, V, O, L})) != ATTN_OK) return st;
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv;
+  if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s))
+    return ATTN_ERR_CUDA;
+  return cuda_status(launch_fwd(mq, mk, mv, O, L, s, scale, err, (cudaStream_t)stream));
+}
+
+int attn_bwd_preprocess(const void* O, const void* dO, const float* L, int B, int H, int N, int d,
+                        void* workspace, size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, 0, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({O, dO, L})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  return cuda_status(launch_bwd_preprocess(O, dO, L, carve_workspace(workspace, s), s,
+                                           (cudaStream_t)stream));
+}
+
+int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
+                  int B, int H, int N, int d, int causal, float scale, void* workspace,
+                  size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q, K, V, dO, dK, dV})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo;
+  if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s) ||
+      make_tile_map(&mdo, dO, s))
+    return ATTN_ERR_CUDA;
+  return cuda_status(launch_bwd_main(mq, mk, mv, mdo, dK, dV, carve_workspace(workspace, s), s,
+                                     scale, err, (cudaStream_t)stream));
+}
+
+int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
+                        size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, 0, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({dQ})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  return cuda_status(launch_bwd_dq_convert(dQ, carve_workspace(const_cast<void*>(workspace), s),
+                                           s, scale, (cudaStream_t)stream));
+}
+
+int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+             const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal,
+             float scale, void* workspace, size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q, K, V, O, dO, L, dQ, dK, dV})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  st = attn_bwd_preprocess(O, dO, L, B, H, N, d, workspace, workspace_bytes_, stream);
+  if (st != ATTN_OK) return st;
+  st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, causal, scale, workspace, workspace_bytes_,
+                     stream);
+  if (st != ATTN_OK) return st;
+  return attn_bwd_dq_convert(dQ, B, H, N, d, scale, workspace, workspace_bytes_, stream);
+}
+
+int attn_device_error_word(void* stream, int* word) {
+  if (word) *word = 0;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (host != 0 && cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word) *word = host;
+  if (host == 0) return ATTN_OK;
+  return (host >> 24) == kDevTimeout ? ATTN_ERR_TIMEOUT : ATTN_ERR_DEVICE;
+}
+
+int attn_last_device_error(void* stream) { return attn_device_error_word(stream, nullptr); }
+
+int attn_watchdog_selftest(uint64_t limit_ns, void* stream) {
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  return cuda_status(launch_watchdog_selftest(err, limit_ns, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,535 @@
+// attn_bwd.cu -- exact-attention backward on sm_103a.
+//
+// The FlashAttention-2 backward of "Training Transformers and Hybrid models
+// on AMD Instinct MI300X Accelerators" (section "Flash Attention"), with the
+// forward's probabilities recomputed instead of stored (section "Harnessing
+// the MI300 Hardware Specs": the backward is harder partly because of this
+// activation recomputation).  Three kernels run in stream order:
+//
+//  1. attn_bwd_preprocess_kernel: D_i = <dO_i, O_i>, L_i log2(e), and a zeroed
+//     fp32 dQ accumulator (HBM-bound).
+//  2. attn_bwd_main_kernel: one CTA per (head, 128-row key/value tile), looping
+//     over 128-row query tiles.  Per query tile, five tcgen05.mma contractions:
+//        S^T = K Q^T              (tensor memory, 128 x 128 fp32)
+//        P^T = 2^(S^T s log2e - L log2e)    softmax warps, written back as bf16
+//        dP^T = V dO^T            (tensor memory)
+//        dV  += P^T dO            (A operand read from tensor memory)
+//        dS^T = P^T o (dP^T - D)  softmax warps, bf16 into shared memory
+//        dK  += dS^T Q
+//        dQ_i = dS K              (tensor memory, then fp32 vector reductions
+//                                  into the accumulator)
+//     dK and dV stay in tensor memory for the whole loop and are written once.
+//  3. attn_bwd_dq_convert_kernel: dQ = bf16(s * accumulator) (HBM-bound).
+//
+// Warp roles of the main kernel (14 warps): 0-3 drain dQ from tensor memory
+// into the accumulator; 4-7 and 8-11 each own 64 of the 128 query columns of
+// S^T/dP^T (one key row = one tensor-memory lane per thread); 12 issues TMA;
+// 13 issues tcgen05.mma and owns the tensor-memory allocation.  Tensor memory
+// (512 columns): dV | dK | S^T (P^T) | dP^T (later dQ).  Shared memory: K, V,
+// two stages of Q and dO, the dS^T tile and the per-row L and D vectors.
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace bwd {
+
+constexpr int kThreads = 448;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr uint32_t kTmemCols = 512;
+
+constexpr int kBarKV = 0;
+constexpr int kBarQFull = 1;     // + stage
+constexpr int kBarQEmpty = 3;    // + stage
+constexpr int kBarDOFull = 5;    // + stage
+constexpr int kBarDOEmpty = 7;   // + stage
+constexpr int kBarSFull = 9;
+constexpr int kBarPReady = 10;
+constexpr int kBarDPFull = 11;
+constexpr int kBarDSReady = 12;
+constexpr int kBarDSFree = 13;
+constexpr int kBarDQFull = 14;
+constexpr int kBarDQFree = 15;
+constexpr int kBarAccFull = 16;
+constexpr int kBarDrain = 17;
+constexpr int kNumBars = 18;
+
+template <int HD>
+struct Layout {
+  static constexpr int kTileBytes = 128 * HD * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;          // + stage * kTileBytes
+  static constexpr int kDO = kQ + 2 * kTileBytes;     // + stage * kTileBytes
+  static constexpr int kDS = kDO + 2 * kTileBytes;    // 128 x 128 bf16, two 16 KB blocks
+  static constexpr int kVec = kDS + 32768;            // stage s: L2 at +1024 s, D at +1024 s + 512
+  static constexpr int kBar = kVec + 2048;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  // At least half of the SM's shared memory: one CTA (owning all 512
+  // tensor-memory columns) per SM.
+  static constexpr int kRaw = (kAbort + 4 + 15) / 16 * 16;
+  static constexpr int kBytes = kRaw > 118784 ? kRaw : 118784;
+  static constexpr uint32_t kColDV = 0;
+  static constexpr uint32_t kColDK = HD;
+  static constexpr uint32_t kColS = 2 * HD;
+  static constexpr uint32_t kColDP = 2 * HD + 128;
+};
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int k) {
+  return make_sdesc_sw128(tile + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int k) {
+  return make_sdesc_sw128(tile + k * 2048, 16384, 1024);
+}
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmdO, const float* __restrict__ L2ws,
+                         const float* __restrict__ Dws, float* __restrict__ acc,
+                         __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int BH,
+                         int N, float scale, float scale_log2, int* err) {
+  using Ly = Layout<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) report_error(err, kDevSmemAlign, 0x200);
+    return;
+  }
+
+  const int n_tiles = (N + 127) >> 7;
+  const int Npad = n_tiles * 128;
+  const int bh = blockIdx.x % BH;
+  const int jt = blockIdx.x / BH;          // key/value tile (small first: heaviest when causal)
+  const int it0 = CAUSAL ? jt : 0;         // first query tile that sees this key tile
+  const int n_it = n_tiles - it0;
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
+  auto bar = [&](int i) -> uint32_t { return sbase + Ly::kBar + 8 * i; };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(kBarKV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarQFull + s), 1);
+      mbar_init(bar(kBarQEmpty + s), 1);
+      mbar_init(bar(kBarDOFull + s), 1);
+      mbar_init(bar(kBarDOEmpty + s), 1);
+    }
+    mbar_init(bar(kBarSFull), 1);
+    mbar_init(bar(kBarPReady), 256);
+    mbar_init(bar(kBarDPFull), 1);
+    mbar_init(bar(kBarDSReady), 256);
+    mbar_init(bar(kBarDSFree), 1);
+    mbar_init(bar(kBarDQFull), 1);
+    mbar_init(bar(kBarDQFree), 128);
+    mbar_init(bar(kBarAccFull), 1);
+    mbar_init(bar(kBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const WaitCtx ctx{abort_flag, err, kWaitLimitNs};
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(kBarKV), 2 * Ly::kTileBytes);
+      for (int cb = 0; cb < HD / 64; ++cb) {
+        tma_load_3d(sbase + Ly::kK + cb * 16384, &tmK, bar(kBarKV), cb * 64, jt * 128, bh);
+        tma_load_3d(sbase + Ly::kV + cb * 16384, &tmV, bar(kBarKV), cb * 64, jt * 128, bh);
+      }
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1, n = it >> 1, qt = it0 + it;
+        if (it >= 2 && !mbar_wait(bar(kBarQEmpty + s), (n - 1) & 1, ctx, 0x210)) break;
+        mbar_arrive_expect_tx(bar(kBarQFull + s), Ly::kTileBytes + 1024);
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(sbase + Ly::kQ + s * Ly::kTileBytes + cb * 16384, &tmQ, bar(kBarQFull + s),
+                      cb * 64, qt * 128, bh);
+        const size_t vo = size_t(bh) * Npad + size_t(qt) * 128;
+        bulk_load(sbase + Ly::kVec + s * 1024, L2ws + vo, 512, bar(kBarQFull + s));
+        bulk_load(sbase + Ly::kVec + s * 1024 + 512, Dws + vo, 512, bar(kBarQFull + s));
+        if (it >= 2 && !mbar_wait(bar(kBarDOEmpty + s), (n - 1) & 1, ctx, 0x211)) break;
+        mbar_arrive_expect_tx(bar(kBarDOFull + s), Ly::kTileBytes);
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(sbase + Ly::kDO + s * Ly::kTileBytes + cb * 16384, &tmdO,
+                      bar(kBarDOFull + s), cb * 64, qt * 128, bh);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+      constexpr uint32_t kIdV = make_idesc_bf16(128, HD, 0, 1);    // dV, dK
+      constexpr uint32_t kIdQ = make_idesc_bf16(128, HD, 1, 1);    // dQ = dS K
+      const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV, sDS = sbase + Ly::kDS;
+      const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
+      const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
+      bool ok = mbar_wait(bar(kBarKV), 0, ctx, 0x220);
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it & 1, ph = (it >> 1) & 1;
+        const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
+        const uint32_t sDO = sbase + Ly::kDO + s * Ly::kTileBytes;
+        // S^T = K Q^T
+        if (!(ok = mbar_wait(bar(kBarQFull + s), ph, ctx, 0x221))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tS, kmajor_desc(sK, k), kmajor_desc(sQ, k), kIdS, k > 0);
+        tc_commit(bar(kBarSFull));
+        // dP^T = V dO^T  (its columns held dQ of the previous tile: wait for the drain)
+        if (!(ok = mbar_wait(bar(kBarDOFull + s), ph, ctx, 0x222))) break;
+        if (it > 0 && !(ok = mbar_wait(bar(kBarDQFree), (it - 1) & 1, ctx, 0x223))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(tDP, kmajor_desc(sV, k), kmajor_desc(sDO, k), kIdS, k > 0);
+        tc_commit(bar(kBarDPFull));
+        // dV += P^T dO, P^T read from tensor memory: query block k/4 was packed by
+        // the softmax warps of that half into its own first 32 columns.
+        if (!(ok = mbar_wait(bar(kBarPReady), it & 1, ctx, 0x224))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tDV, tS + 64 * (k >> 2) + 8 * (k & 3), mnmajor_desc(sDO, k), kIdV,
+                 (it > 0 || k > 0) ? 1u : 0u);
+        tc_commit(bar(kBarDOEmpty + s));
+        // dK += dS^T Q, then dQ_i = dS K into the dP^T columns
+        if (!(ok = mbar_wait(bar(kBarDSReady), it & 1, ctx, 0x225))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tDK, kmajor_desc(sDS, k), mnmajor_desc(sQ, k), kIdV, (it > 0 || k > 0) ? 1u : 0u);
+        tc_commit(bar(kBarQEmpty + s));
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tDP, mnmajor_desc(sDS, k), mnmajor_desc(sK, k), kIdQ, k > 0);
+        tc_commit(bar(kBarDQFull));
+        tc_commit(bar(kBarDSFree));
+      }
+      tc_commit(bar(kBarAccFull));
+      tc_commit(bar(kBarDrain));
+      volatile int never = 0;
+      const WaitCtx own{&never, err, kWaitLimitNs};
+      mbar_wait(bar(kBarDrain), 0, own, 0x22F);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / dS
+    const int h = (warp - 4) >> 2;       // query half: columns 64h .. 64h+63
+    const int r = threadIdx.x & 127;     // key row within the tile = TMEM lane
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_off + Ly::kColS + 64 * h;
+    const uint32_t tDP = tbase + lane_off + Ly::kColDP + 64 * h;
+    const uint32_t sDSrow = sbase + Ly::kDS + h * 16384 + r * 128;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1, qt = it0 + it;
+      if (!(ok = mbar_wait_warp(bar(kBarQFull + s), (it >> 1) & 1, ctx, 0x230))) break;
+      if (!(ok = mbar_wait_warp(bar(kBarSFull), it & 1, ctx, 0x231))) break;
+      tc_fence_after();
+      const float* L2v = reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024) + 64 * h;
+      const float* Dv = reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024 + 512) + 64 * h;
+      {
+        uint32_t u[64];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        const bool diag = CAUSAL && qt == jt;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c2 = 0; c2 < 32; ++c2) {
+          float p0 = ex2(fmaf(__uint_as_float(u[2 * c2]), scale_log2, -L2v[2 * c2]));
+          float p1 = ex2(fmaf(__uint_as_float(u[2 * c2 + 1]), scale_log2, -L2v[2 * c2 + 1]));
+          if (diag) {  // key row r is visible to query columns >= r only
+            if (64 * h + 2 * c2 < r) p0 = 0.f;
+            if (64 * h + 2 * c2 + 1 < r) p1 = 0.f;
+          }
+          pk[c2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPReady));
+      }
+      if (!(ok = mbar_wait_warp(bar(kBarDPFull), it & 1, ctx, 0x232))) break;
+      if (it > 0 && !(ok = mbar_wait_warp(bar(kBarDSFree), (it - 1) & 1, ctx, 0x233))) break;
+      tc_fence_after();
+      {
+        uint32_t u[64], pk[32];
+        tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_ld32(tS, pk);
+        tmem_wait_ld();
+        uint32_t ds[32];
+#pragma unroll
+        for (int c2 = 0; c2 < 32; ++c2) {
+          const float p0 = bf16lo_to_f32(pk[c2]), p1 = bf16hi_to_f32(pk[c2]);
+          const float ds0 = p0 * (__uint_as_float(u[2 * c2]) - Dv[2 * c2]);
+          const float ds1 = p1 * (__uint_as_float(u[2 * c2 + 1]) - Dv[2 * c2 + 1]);
+          ds[c2] = pack_bf16x2(ds0, ds1);
+        }
+        // Row r of the dS^T tile, 128-byte swizzle: 16-byte chunk c lands at c ^ (r % 8).
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(sDSrow + ((c ^ (r & 7)) << 4), ds[4 * c], ds[4 * c + 1], ds[4 * c + 2],
+                       ds[4 * c + 3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(kBarDSReady));
+      }
+    }
+    // Epilogue: half 0 writes dV, half 1 writes dK (times the softmax scale).
+    if (ok && mbar_wait_warp(bar(kBarAccFull), 0, ctx, 0x238 + h)) {
+      tc_fence_after();
+      const int kv = jt * 128 + r;
+      const uint32_t tAcc = tbase + lane_off + (h == 0 ? Ly::kColDV : Ly::kColDK);
+      const float mult = h == 0 ? 1.f : scale;
+      __nv_bfloat16* orow = (h == 0 ? dV : dK) + (size_t(bh) * N + kv) * HD;
+#pragma unroll
+      for (int c4 = 0; c4 < HD / 32; ++c4) {
+        uint32_t o[32];
+        tmem_ld32(tAcc + 32 * c4, o);
+        tmem_wait_ld();
+        if (kv < N) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = pack_bf16x2(__uint_as_float(o[8 * c8 + 2 * e]) * mult,
+                                  __uint_as_float(o[8 * c8 + 2 * e + 1]) * mult);
+            st_global_v4(orow + 32 * c4 + 8 * c8, w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int r = threadIdx.x;  // query row within the tile = TMEM lane
+    const uint32_t tDQ = tbase + (uint32_t(warp * 32) << 16) + Ly::kColDP;
+    for (int it = 0; it < n_it; ++it) {
+      const int qt = it0 + it;
+      if (!mbar_wait_warp(bar(kBarDQFull), it & 1, ctx, 0x240)) break;
+      tc_fence_after();
+      // accumulator layout [bh][tile][HD/8][128][8]
+      float* abase = acc + (size_t(bh) * n_tiles + qt) * (HD / 8) * 1024 + r * 8;
+#pragma unroll
+      for (int half = 0; half < HD / 64; ++half) {
+        uint32_t u[64];
+        tmem_ld32(tDQ + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tDQ + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_wait_ld();
+        if (half == HD / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(kBarDQFree));
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          float* p = abase + (half * 8 + g) * 1024;
+          red_add_v4(p, __uint_as_float(u[8 * g]), __uint_as_float(u[8 * g + 1]),
+                     __uint_as_float(u[8 * g + 2]), __uint_as_float(u[8 * g + 3]));
+          red_add_v4(p + 4, __uint_as_float(u[8 * g + 4]), __uint_as_float(u[8 * g + 5]),
+                     __uint_as_float(u[8 * g + 6]), __uint_as_float(u[8 * g + 7]));
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  if (*abort_flag && threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ step 1
+// One row per HD/8 threads (16 bytes each); rows beyond N get D = 0 and
+// L2 = +inf so that their recomputed probabilities are exactly 0.
+template <int HD>
+__global__ void __launch_bounds__(256)
+    attn_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ O,
+                               const __nv_bfloat16* __restrict__ dO, const float* __restrict__ L,
+                               float* __restrict__ L2ws, float* __restrict__ Dws,
+                               float* __restrict__ acc, int BH, int N, int Npad,
+                               size_t acc_vec4) {
+  constexpr int TPR = HD / 8;  // threads per row
+  const size_t rows = size_t(BH) * Npad;
+  const size_t nthreads = size_t(gridDim.x) * blockDim.x;
+  const size_t gt = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  // rows: grid-stride in whole warps so the shuffle groups stay aligned
+  for (size_t base = (gt / 32) * 32; base < rows * TPR; base += nthreads) {
+    const size_t id = base + (gt & 31);
+    const size_t row = id / TPR;
+    const int sub = int(id % TPR);
+    float dot = 0.f;
+    const bool in = row < rows;
+    const int bh = in ? int(row / Npad) : 0;
+    const int q = in ? int(row % Npad) : 0;
+    const bool valid = in && q < N;
+    if (valid) {
+      const size_t off = (size_t(bh) * N + q) * HD + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(O + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(dO + off);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dot += bf16lo_to_f32(av[e]) * bf16lo_to_f32(bv[e]) +
+               bf16hi_to_f32(av[e]) * bf16hi_to_f32(bv[e]);
+    }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (in && sub == 0) {
+      Dws[row] = valid ? dot : 0.f;
+      L2ws[row] = valid ? L[size_t(bh) * N + q] * 1.4426950408889634f : INFINITY;
+    }
+  }
+  float4* a4 = reinterpret_cast<float4*>(acc);
+  for (size_t i = gt; i < acc_vec4; i += nthreads) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------ step 3
+template <int HD>
+__global__ void __launch_bounds__(256)
+    attn_bwd_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dQ,
+                               int BH, int N, int n_tiles, float scale) {
+  const size_t units = size_t(BH) * n_tiles * (HD / 8) * 128;
+  const size_t nthreads = size_t(gridDim.x) * blockDim.x;
+  for (size_t u = size_t(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += nthreads) {
+    const int r = int(u & 127);
+    const size_t rest = u >> 7;
+    const int g = int(rest % (HD / 8));
+    const size_t bt = rest / (HD / 8);
+    const int qt = int(bt % n_tiles);
+    const int bh = int(bt / n_tiles);
+    const int q = qt * 128 + r;
+    if (q >= N) continue;
+    const float4 a = *reinterpret_cast<const float4*>(acc + u * 8);
+    const float4 b = *reinterpret_cast<const float4*>(acc + u * 8 + 4);
+    st_global_v4(dQ + (size_t(bh) * N + q) * HD + g * 8, pack_bf16x2(a.x * scale, a.y * scale),
+                 pack_bf16x2(a.z * scale, a.w * scale), pack_bf16x2(b.x * scale, b.y * scale),
+                 pack_bf16x2(b.z * scale, b.w * scale));
+  }
+}
+
+// ------------------------------------------------------------------ self-test
+// A wait that nothing can satisfy: the bounded wait must give up, record a
+// timeout and let the kernel exit normally.
+__global__ void attn_watchdog_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t barrier;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&barrier), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitCtx ctx{&abort_flag, err, limit_ns};
+  mbar_wait(smem_u32(&barrier), 0, ctx, 0xD06);
+}
+
+template <int HD, bool CAUSAL>
+static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO, void* dK,
+                                 void* dV, const Workspace& ws, const Shape& s, float scale,
+                                 int* err, cudaStream_t stream) {
+  using Ly = Layout<HD>;
+  auto kern = attn_bwd_main_kernel<HD, CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(unsigned(s.n_tiles) * unsigned(s.BH));
+  kern<<<grid, kThreads, Ly::kBytes, stream>>>(
+      tmQ, tmK, tmV, tmdO, ws.L2, ws.D, ws.acc, reinterpret_cast<__nv_bfloat16*>(dK),
+      reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, scale, scale * 1.4426950408889634f, err);
+  return cudaGetLastError();
+}
+
+static unsigned grid_for(size_t work_items, int per_block) {
+  size_t blocks = (work_items + per_block - 1) / per_block;
+  const size_t cap = 152 * 16;  // a few full waves of 256-thread blocks
+  if (blocks > cap) blocks = cap;
+  return unsigned(blocks > 0 ? blocks : 1);
+}
+
+}  // namespace bwd
+
+cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
+                                  const Workspace& ws, const Shape& s, cudaStream_t stream) {
+  const size_t rows = size_t(s.BH) * s.Npad;
+  const size_t acc_vec4 = size_t(s.BH) * s.Npad * s.d / 4;
+  const size_t work = rows * (s.d / 8) > acc_vec4 ? rows * (s.d / 8) : acc_vec4;
+  const unsigned grid = bwd::grid_for(work, 256);
+  auto o = reinterpret_cast<const __nv_bfloat16*>(O);
+  auto g = reinterpret_cast<const __nv_bfloat16*>(dO);
+  if (s.d == 64)
+    bwd::attn_bwd_preprocess_kernel<64>
+        <<<grid, 256, 0, stream>>>(o, g, L, ws.L2, ws.D, ws.acc, s.BH, s.N, s.Npad, acc_vec4);
+  else
+    bwd::attn_bwd_preprocess_kernel<128>
+        <<<grid, 256, 0, stream>>>(o, g, L, ws.L2, ws.D, ws.acc, s.BH, s.N, s.Npad, acc_vec4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO, void* dK, void* dV,
+                            const Workspace& ws, const Shape& s, float scale, int* err,
+                            cudaStream_t stream) {
+  if (s.d == 64)
+    return s.causal
+               ? bwd::launch_main_t<64, true>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err, stream)
+               : bwd::launch_main_t<64, false>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err,
+                                               stream);
+  return s.causal
+             ? bwd::launch_main_t<128, true>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err, stream)
+             : bwd::launch_main_t<128, false>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err,
+                                              stream);
+}
+
+cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,
+                                  cudaStream_t stream) {
+  const size_t units = size_t(s.BH) * s.n_tiles * (s.d / 8) * 128;
+  const unsigned grid = bwd::grid_for(units, 256);
+  auto q = reinterpret_cast<__nv_bfloat16*>(dQ);
+  if (s.d == 64)
+    bwd::attn_bwd_dq_convert_kernel<64><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N,
+                                                                  s.n_tiles, scale);
+  else
+    bwd::attn_bwd_dq_convert_kernel<128><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N,
+                                                                   s.n_tiles, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_watchdog_selftest(int* err, uint64_t limit_ns, cudaStream_t stream) {
+  bwd::attn_watchdog_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

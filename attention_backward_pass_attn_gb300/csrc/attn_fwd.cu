@@ -1,0 +1,369 @@
+// attn_fwd.cu -- exact-attention forward on sm_103a: O = softmax(s Q K^T) V and
+// the row log-sum-exp L, never storing the N x N score matrix.
+//
+// This is the forward the backward consumes (FlashAttention-2 forward, page
+// "Training Transformers and Hybrid models on AMD Instinct MI300X
+// Accelerators", section "Flash Attention").  Design for GB300:
+//
+//  * One CTA owns two 128-row query tiles of one head (A and B) and streams
+//    128-row K/V tiles through a two-stage TMA ring.  Both query tiles reuse
+//    every K/V tile that lands in shared memory.
+//  * Warp roles: warps 0-3 run the softmax of tile A, warps 4-7 that of tile
+//    B (one thread per query row = one TMEM lane), warp 8 issues TMA copies,
+//    warp 9 issues tcgen05.mma and owns the tensor-memory allocation.
+//  * Tensor memory (512 columns x 128 lanes, fp32): O_A, O_B (d columns each)
+//    and S_A, S_B (128 columns each).  S = Q K^T lands in S_x; the softmax
+//    threads overwrite its first 64 columns with P in bf16 (two per column),
+//    and the tensor core reads P straight from tensor memory for O += P V.
+//  * Online softmax in base 2 (log2(e) folded into the scale) with lazy
+//    rescaling: the running maximum is only moved (and O rescaled in tensor
+//    memory) when it grows by more than 2^8, which keeps P <= 256.
+//  * While the softmax of tile A runs, the tensor core works on tile B, and
+//    the next S of one tile is computed while the other tile's P V runs.
+//  * Causal: a CTA stops at the last key tile its rows can see; tiles on the
+//    diagonal are masked element-wise.  CTAs are launched heaviest first.
+//  * Every mbarrier wait is bounded (see ptx.cuh); on expiry the kernel
+//    records an error, drains the tensor core and exits normally.
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace fwd {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kStages = 2;
+constexpr uint32_t kTmemCols = 512;
+
+// Barrier indices.
+constexpr int kBarQFull = 0;
+constexpr int kBarKFull = 1;                       // + stage
+constexpr int kBarKEmpty = kBarKFull + kStages;    // + stage
+constexpr int kBarVFull = kBarKEmpty + kStages;    // + stage
+constexpr int kBarVEmpty = kBarVFull + kStages;    // + stage
+constexpr int kBarSFull = kBarVEmpty + kStages;    // + tile (0 = A, 1 = B)
+constexpr int kBarPReady = kBarSFull + 2;          // + tile
+constexpr int kBarOFull = kBarPReady + 2;
+constexpr int kBarDrain = kBarOFull + 1;
+constexpr int kNumBars = kBarDrain + 1;
+
+template <int HD>
+struct Layout {
+  static constexpr int kTileBytes = 128 * HD * 2;   // one 128-row bf16 tile
+  static constexpr int kQ = 0;                       // two query tiles
+  static constexpr int kK = kQ + 2 * kTileBytes;     // kStages key tiles
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  // Padded past half of the SM's shared memory so that at most one CTA (which
+  // allocates all 512 tensor-memory columns) is resident per SM.
+  static constexpr int kRaw = (kAbort + 4 + 15) / 16 * 16;
+  static constexpr int kBytes = kRaw > 118784 ? kRaw : 118784;
+  // tensor-memory columns
+  static constexpr uint32_t kColO = 0;           // + tile * HD
+  static constexpr uint32_t kColS = 2 * HD;      // + tile * 128
+};
+
+// K-major operand, 128-byte swizzle: K-step k (16 bf16) of a tile whose rows
+// hold HD contiguous values split in 64-column blocks of 16 KB.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int k) {
+  return make_sdesc_sw128(tile + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+}
+// MN-major operand: K-step k covers tile rows 16k..16k+15; the MN extent runs
+// along the row, across 64-column blocks 16 KB apart.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int k) {
+  return make_sdesc_sw128(tile + k * 2048, 16384, 1024);
+}
+
+template <int HD, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                    float* __restrict__ Lout, int BH, int N, float scale_log2, int* err) {
+  using Ly = Layout<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (sbase & 1023u) {  // uniform over the CTA: every thread returns here
+    if (threadIdx.x == 0) report_error(err, kDevSmemAlign, 0x100);
+    return;
+  }
+
+  const int n_tiles = (N + 127) >> 7;
+  const int n_pairs = (n_tiles + 1) >> 1;
+  const int bh = blockIdx.x % BH;
+  const int pair = CAUSAL ? (n_pairs - 1 - int(blockIdx.x / BH)) : int(blockIdx.x / BH);
+  const int qt_a = 2 * pair;
+  const bool has_b = qt_a + 1 < n_tiles;
+  const int n_kv = CAUSAL ? min(n_tiles, qt_a + (has_b ? 2 : 1)) : n_tiles;
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
+  auto bar = [&](int i) -> uint32_t { return sbase + Ly::kBar + 8 * i; };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(kBarQFull), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarPReady + t), 128);
+    }
+    mbar_init(bar(kBarOFull), 1);
+    mbar_init(bar(kBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const WaitCtx ctx{abort_flag, err, kWaitLimitNs};
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(kBarQFull), (has_b ? 2 : 1) * Ly::kTileBytes);
+      for (int t = 0; t < (has_b ? 2 : 1); ++t)
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(sbase + Ly::kQ + t * Ly::kTileBytes + cb * 16384, &tmQ, bar(kBarQFull),
+                      cb * 64, (qt_a + t) * 128, bh);
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % kStages, n = j / kStages;
+        if (j >= kStages && !mbar_wait(bar(kBarKEmpty + s), (n - 1) & 1, ctx, 0x110)) break;
+        mbar_arrive_expect_tx(bar(kBarKFull + s), Ly::kTileBytes);
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(sbase + Ly::kK + s * Ly::kTileBytes + cb * 16384, &tmK,
+                      bar(kBarKFull + s), cb * 64, j * 128, bh);
+        if (j >= kStages && !mbar_wait(bar(kBarVEmpty + s), (n - 1) & 1, ctx, 0x111)) break;
+        mbar_arrive_expect_tx(bar(kBarVFull + s), Ly::kTileBytes);
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(sbase + Ly::kV + s * Ly::kTileBytes + cb * 16384, &tmV,
+                      bar(kBarVFull + s), cb * 64, j * 128, bh);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);  // S = Q K^T
+      constexpr uint32_t kIdO = make_idesc_bf16(128, HD, 0, 1);   // O += P V
+      auto issue_s = [&](int t, int stage) {
+        const uint32_t qa = sbase + Ly::kQ + t * Ly::kTileBytes;
+        const uint32_t ka = sbase + Ly::kK + stage * Ly::kTileBytes;
+        const uint32_t d = tbase + Ly::kColS + 128 * t;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          mma_ss(d, kmajor_desc(qa, k), kmajor_desc(ka, k), kIdS, k > 0);
+        tc_commit(bar(kBarSFull + t));
+      };
+      auto issue_pv = [&](int t, int stage, bool acc) {
+        const uint32_t va = sbase + Ly::kV + stage * Ly::kTileBytes;
+        const uint32_t d = tbase + Ly::kColO + HD * t;
+        const uint32_t p = tbase + Ly::kColS + 128 * t;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // 128 keys, 16 per step; P packed 2 per column
+          mma_ts(d, p + 8 * k, mnmajor_desc(va, k), kIdO, (acc || k > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(kBarQFull), 0, ctx, 0x120) &&
+                mbar_wait(bar(kBarKFull), 0, ctx, 0x121);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        if (has_b) issue_s(1, 0);
+        tc_commit(bar(kBarKEmpty));
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int s = j % kStages;
+          const bool next = j + 1 < n_kv;
+          const int s1 = (j + 1) % kStages, n1 = (j + 1) / kStages;
+          if (!(ok = mbar_wait(bar(kBarVFull + s), (j / kStages) & 1, ctx, 0x122))) break;
+          if (!(ok = mbar_wait(bar(kBarPReady + 0), j & 1, ctx, 0x123))) break;
+          tc_fence_after();
+          issue_pv(0, s, j > 0);
+          if (next) {
+            if (!(ok = mbar_wait(bar(kBarKFull + s1), n1 & 1, ctx, 0x124))) break;
+            tc_fence_after();
+            issue_s(0, s1);
+          }
+          if (has_b) {
+            if (!(ok = mbar_wait(bar(kBarPReady + 1), j & 1, ctx, 0x125))) break;
+            tc_fence_after();
+            issue_pv(1, s, j > 0);
+            if (next) issue_s(1, s1);
+          }
+          tc_commit(bar(kBarVEmpty + s));
+          if (next) tc_commit(bar(kBarKEmpty + s1));
+        }
+        tc_commit(bar(kBarOFull));
+      }
+      // Wait until every MMA issued above has completed before teardown.
+      tc_commit(bar(kBarDrain));
+      volatile int never = 0;  // this wait ignores the CTA abort flag
+      const WaitCtx own{&never, err, kWaitLimitNs};
+      mbar_wait(bar(kBarDrain), 0, own, 0x12F);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;  // 0 = tile A, 1 = tile B
+    const int r = threadIdx.x & 127;
+    if (t == 0 || has_b) {
+      const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+      const uint32_t tS = tbase + lane_off + Ly::kColS + 128 * t;
+      const uint32_t tO = tbase + lane_off + Ly::kColO + HD * t;
+      const int q_tile0 = (qt_a + t) * 128;
+      const int q = q_tile0 + r;
+      float m = -INFINITY;  // running max of the base-2 scaled scores
+      float l = 0.f;        // running sum of 2^(x - m)
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        if (!(ok = mbar_wait_warp(bar(kBarSFull + t), j & 1, ctx, 0x130 + t))) break;
+        tc_fence_after();
+        uint32_t u[128];
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
+        tmem_wait_ld();
+        const int kv0 = j * 128;
+        if ((CAUSAL && kv0 + 127 > q_tile0) || kv0 + 128 > N) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int kv = kv0 + c;
+            if ((CAUSAL && kv > q) || kv >= N) u[c] = __float_as_uint(-INFINITY);
+          }
+        }
+        float mx = __uint_as_float(u[0]);
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(u[c]));
+        const float mt = mx * scale_log2;  // scale > 0, so the max commutes with it
+        const float m_new = fmaxf(m, mt);
+        // Lazy rescale: move the reference maximum (and rescale l and O by
+        // 2^(m - m_new)) only when the maximum grew by more than 8 in base 2.
+        const bool rescale = m_new > m + 8.f;
+        const float alpha = rescale ? ex2(m - m_new) : 1.f;
+        if (rescale) {
+          l *= alpha;
+          m = m_new;
+        }
+        const float mb = (m == -INFINITY) ? 0.f : m;
+        float rowsum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2) {
+            const float p0 = ex2(fmaf(__uint_as_float(u[64 * h + 2 * c2]), scale_log2, -mb));
+            const float p1 = ex2(fmaf(__uint_as_float(u[64 * h + 2 * c2 + 1]), scale_log2, -mb));
+            rowsum += p0 + p1;
+            pk[c2] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + 32 * h, pk);
+        }
+        l += rowsum;
+        // tcgen05.ld/st are warp-collective: if any row of the warp moved its
+        // maximum, the whole warp rescales (alpha = 1 leaves the other rows
+        // unchanged).  O holds P V of earlier tiles; PV(j-1) has completed.
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c4 = 0; c4 < HD / 32; ++c4) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c4, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tO + 32 * c4, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPReady + t));
+      }
+      if (ok && mbar_wait_warp(bar(kBarOFull), 0, ctx, 0x138 + t)) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        __nv_bfloat16* orow = O + (size_t(bh) * N + q) * HD;
+#pragma unroll
+        for (int c4 = 0; c4 < HD / 32; ++c4) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c4, o);
+          tmem_wait_ld();
+          if (q < N) {
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16x2(__uint_as_float(o[8 * c8 + 2 * e]) * inv_l,
+                                    __uint_as_float(o[8 * c8 + 2 * e + 1]) * inv_l);
+              st_global_v4(orow + 32 * c4 + 8 * c8, w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+        if (q < N) Lout[size_t(bh) * N + q] = (m + log2f(l)) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  if (*abort_flag && threadIdx.x == 0) {
+    // Give copies still in flight time to land before the CTA retires.
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int HD, bool CAUSAL>
+static cudaError_t launch_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, void* O, float* L, const Shape& s,
+                            float scale, int* err, cudaStream_t stream) {
+  using Ly = Layout<HD>;
+  auto kern = attn_fwd_kernel<HD, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  if (e != cudaSuccess) return e;
+  const int n_pairs = (s.n_tiles + 1) / 2;
+  const dim3 grid(unsigned(n_pairs) * unsigned(s.BH));
+  const float scale_log2 = scale * 1.4426950408889634f;
+  kern<<<grid, kThreads, Ly::kBytes, stream>>>(tmQ, tmK, tmV,
+                                               reinterpret_cast<__nv_bfloat16*>(O), L, s.BH, s.N,
+                                               scale_log2, err);
+  return cudaGetLastError();
+}
+
+}  // namespace fwd
+
+cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       void* O, float* L, const Shape& s, float scale, int* err,
+                       cudaStream_t stream) {
+  if (s.d == 64)
+    return s.causal ? fwd::launch_t<64, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
+                    : fwd::launch_t<64, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+  return s.causal ? fwd::launch_t<128, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
+                  : fwd::launch_t<128, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+}
+
+}  // namespace attn

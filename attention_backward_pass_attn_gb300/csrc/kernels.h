@@ -1,0 +1,56 @@
+// kernels.h -- host-side launchers shared between the kernel translation units
+// and the C ABI in attn_api.cu.  Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace attn {
+
+// One attention problem: BH = B*H independent heads of N rows, head dim d.
+struct Shape {
+  int BH;
+  int N;
+  int d;
+  int causal;
+  int n_tiles;  // ceil(N / 128): 128-row tiles per head
+  int Npad;     // n_tiles * 128
+};
+
+// Workspace carve-up (all fp32, 256-byte aligned sections):
+//   L2  [BH][Npad]            L * log2(e); +inf on padded rows
+//   D   [BH][Npad]            rowsum(dO o O); 0 on padded rows
+//   acc [BH][n_tiles][d/8][128][8]   dQ accumulator (unscaled)
+struct Workspace {
+  float* L2;
+  float* D;
+  float* acc;
+};
+
+size_t workspace_bytes(const Shape& s);
+Workspace carve_workspace(void* base, const Shape& s);
+
+// Encodes a 3-D bf16 tensor map over a contiguous [BH][N][d] tensor with a
+// 64 x 128 x 1 box and 128-byte swizzle.  Returns 0 on success.
+int make_tile_map(CUtensorMap* map, const void* ptr, const Shape& s);
+
+cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       void* O, float* L, const Shape& s, float scale, int* err,
+                       cudaStream_t stream);
+
+cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
+                                  const Workspace& ws, const Shape& s, cudaStream_t stream);
+
+cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO, void* dK, void* dV,
+                            const Workspace& ws, const Shape& s, float scale, int* err,
+                            cudaStream_t stream);
+
+cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,
+                                  cudaStream_t stream);
+
+cudaError_t launch_watchdog_selftest(int* err, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,149 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * What it computes.  Exact softmax attention and its fused backward pass, the
+ * "Flash Attention v2" forward and backward kernels named by "Training
+ * Transformers and Hybrid models on AMD Instinct MI300X Accelerators"
+ * (section "Flash Attention"; section "Harnessing the MI300 Hardware Specs"
+ * adds that the backward recomputes the forward's activations).  Per head,
+ * with s = scale and the causal mask keeping key j <= query i:
+ *
+ *   S = s Q K^T (+ mask),  L_i = logsumexp_j S_ij,  P = exp(S - L),  O = P V
+ *   D_i = <dO_i, O_i>,  dP = dO V^T,  dS = P o (dP - D)
+ *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO
+ *
+ * The N x N matrices S, P, dP, dS are never stored: each kernel recomputes
+ * them tile by tile on the tensor cores.
+ *
+ * Layout and types (every entry point).
+ *   Q, K, V, O, dO, dQ, dK, dV : bf16 (raw uint16 bits), contiguous
+ *                                [B][H][N][d], 16-byte aligned.
+ *   L                          : fp32 [B][H][N], natural-log log-sum-exp.
+ *   d                          : 64 or 128.   N: any value >= 0.
+ *   causal                     : 0 or 1 (square, top-left aligned mask).
+ *   scale                      : finite and > 0 (usually 1/sqrt(d)).
+ *   stream                     : a cudaStream_t (NULL = legacy default).
+ * All pointers are DEVICE pointers on the current CUDA device.  The caller
+ * allocates and owns every buffer, the backward's workspace included; the
+ * library allocates no device memory.
+ *
+ * Behaviour.  Arguments are validated on the host before anything is
+ * launched; a bad argument returns an error status and launches nothing.  A
+ * zero B, H or N is a valid empty problem: the call returns ATTN_OK and
+ * launches nothing (pointers may then be NULL).  Otherwise the work is
+ * enqueued on `stream` and the call returns without waiting: inputs must stay
+ * alive and unmodified, and outputs untouched, until the stream reaches the
+ * call.  Kernels never trap: a device-side failure (a bounded wait that ran
+ * out) is recorded in a per-device error word that attn_last_device_error()
+ * reads.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, misaligned pointer */
+  ATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or a size beyond the 32-bit index range */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
+  ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out (reported by attn_last_device_error) */
+  ATTN_ERR_WORKSPACE = 5,   /* workspace NULL, misaligned or smaller than attn_bwd_workspace_size */
+  ATTN_ERR_DEVICE = 6       /* another device-side check failed (see attn_device_error_word) */
+} attn_status_t;
+
+/*
+ * Forward.  O = softmax(scale Q K^T + mask) V and L = row log-sum-exp of the
+ * scaled, masked scores (natural log), as in the forward of the page section
+ * "Flash Attention" (FlashAttention-2).  Writes O [B][H][N][d] bf16 and L
+ * [B][H][N] fp32.  Q, K, V must not alias O.
+ */
+int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+             int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for this shape (0 for an empty
+ * problem).  Holds, per head, D = rowsum(dO o O) and L scaled to base 2, each
+ * [roundup(N,128)] fp32, and an fp32 dQ accumulator of roundup(N,128) x d.
+ * The workspace must be 256-byte aligned; its contents on entry do not matter.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward.  Given the forward's inputs, its outputs O and L, and the
+ * upstream gradient dO, writes dQ, dK, dV (bf16, [B][H][N][d]) -- the
+ * FlashAttention-2 backward of the page section "Flash Attention", with the
+ * probabilities P recomputed from Q, K and L ("activation recomputation",
+ * section "Harnessing the MI300 Hardware Specs").  Runs three kernels on
+ * `stream`: attn_bwd_preprocess, attn_bwd_main and attn_bwd_dq_convert
+ * (below), in that order.  Outputs must not alias inputs or the workspace.
+ */
+int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+             const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+             int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Step 1 of attn_bwd: D_i = <dO_i, O_i> in fp32 and L_i * log2(e) into the
+ * workspace, and zero the workspace's dQ accumulator.  Bound by HBM
+ * bandwidth.
+ */
+int attn_bwd_preprocess(const void* O, const void* dO, const float* L, int B, int H, int N, int d,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Step 2 of attn_bwd: the fused main kernel.  For each 128-row key/value
+ * tile it recomputes S^T = K Q^T and P^T tile by tile, accumulates
+ * dV += P^T dO and dK += dS^T Q in tensor memory, and adds each dQ tile
+ * partial dS K into the workspace's fp32 accumulator.  Writes dK and dV.
+ * Requires attn_bwd_preprocess to have run on the same workspace.
+ */
+int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                  void* dV, int B, int H, int N, int d, int causal, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
+ * Step 3 of attn_bwd: dQ = bf16(scale * accumulator).  Bound by HBM
+ * bandwidth.  Requires attn_bwd_main to have run on the same workspace.
+ */
+int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's error word.
+ * Returns ATTN_OK if no kernel reported a failure since the last call,
+ * ATTN_ERR_TIMEOUT if a bounded wait ran out, ATTN_ERR_DEVICE for another
+ * device-side check, ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+int attn_last_device_error(void* stream);
+
+/*
+ * Like attn_last_device_error, but also stores the raw error word
+ * ((code << 24) | site, 0 if none) in *word before clearing it.
+ */
+int attn_device_error_word(void* stream, int* word);
+
+/*
+ * Failure-detection self-test: launches one tiny kernel whose bounded
+ * mbarrier wait can never be satisfied (nothing arrives), with a limit of
+ * `limit_ns` nanoseconds (1e3 .. 1e10).  The kernel gives up, records
+ * ATTN_ERR_TIMEOUT in the error word and exits normally; it never traps or
+ * hangs.  Returns the launch status.
+ */
+int attn_watchdog_selftest(uint64_t limit_ns, void* stream);
+
+/* Static text for a status code. */
+const char* attn_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

@@ -75,6 +75,11 @@ def load(path: str | None = None):
                                             ctypes.c_double, dp, dp, dp, dp, dp,
                                             dp, ctypes.c_int]
         lib.oracle_attn_fwd_bwd.restype = ctypes.c_int
+        lp = ctypes.POINTER(ctypes.c_long)
+        lib.oracle_attn_head_rows.argtypes = [dp, dp, dp, dp, L, L, ctypes.c_int,
+                                              ctypes.c_double, L, lp, L, lp, dp, dp, dp,
+                                              dp, dp, ctypes.c_int]
+        lib.oracle_attn_head_rows.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         if path is None:
@@ -135,4 +140,30 @@ def attention_forward_backward(q, k, v, do, causal: bool, scale: float,
         _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), int(threads))
     if st != 0:
         raise RuntimeError("oracle_attn_fwd_bwd failed with status %d" % st)
+    return out
+
+
+def attention_head_rows(q, k, v, do, causal: bool, scale: float, q_rows, k_rows,
+                        threads: int = 0, lib=None) -> dict:
+    """Sampled rows of one head ([N, d] inputs), for shapes too large to do in full.
+
+    Returns O, L, dQ at the query rows ``q_rows`` and dK, dV at the key rows
+    ``k_rows`` (float64).  The forward statistics of every row are computed,
+    because dK_j and dV_j depend on L_i and D_i of all query rows.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    if q.ndim != 2 or any(t.shape != q.shape for t in (k, v, do)):
+        raise ValueError("q, k, v, do must share the shape [N, d]")
+    N, d = q.shape
+    qr = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int64)).astype(np.dtype("l"))
+    kr = np.ascontiguousarray(np.asarray(k_rows, dtype=np.int64)).astype(np.dtype("l"))
+    out = {"O": np.zeros((len(qr), d)), "L": np.zeros(len(qr)), "dQ": np.zeros((len(qr), d)),
+           "dK": np.zeros((len(kr), d)), "dV": np.zeros((len(kr), d))}
+    lp = ctypes.POINTER(ctypes.c_long)
+    st = (lib or load()).oracle_attn_head_rows(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, d, int(bool(causal)), float(scale),
+        len(qr), qr.ctypes.data_as(lp), len(kr), kr.ctypes.data_as(lp), _ptr(out["O"]),
+        _ptr(out["L"]), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), int(threads))
+    if st != 0:
+        raise RuntimeError("oracle_attn_head_rows failed with status %d" % st)
     return out

@@ -126,7 +126,49 @@ static int pass_forward(const double *Q, const double *K, const double *V,
   return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 
-/* Pass 2: dQ_i = s * sum_j P_ij (dP_ij - D_i) k_j for every query row. */
+/* dQ_i = s * sum_j P_ij (dP_ij - D_i) k_j for one query row i of one head. */
+static void dq_row(const double *Qh, const double *Kh, const double *Vh,
+                   const double *dOh, const double *Lh, const double *Dh, long N,
+                   long d, int causal, double scale, long i, double *srow,
+                   double *dQi) {
+  const double *dOi = dOh + i * d;
+  long n = scores_row(Qh, Kh, i, N, d, causal, scale, srow);
+  double Li = Lh[i], Di = Dh[i];
+  for (long c = 0; c < d; ++c) dQi[c] = 0.0;
+  for (long j = 0; j < n; ++j) {
+    double p = exp(srow[j] - Li);
+    double dp = dot(dOi, Vh + j * d, d);
+    double ds = p * (dp - Di);
+    const double *kj = Kh + j * d;
+    for (long c = 0; c < d; ++c) dQi[c] += ds * kj[c];
+  }
+  for (long c = 0; c < d; ++c) dQi[c] *= scale;
+}
+
+/* dK_j = s * sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i for one key row j of
+ * one head.  Under the causal mask, key j is seen by query rows i >= j only. */
+static void dkdv_row(const double *Qh, const double *Kh, const double *Vh,
+                     const double *dOh, const double *Lh, const double *Dh, long N,
+                     long d, int causal, double scale, long j, double *dKj,
+                     double *dVj) {
+  const double *kj = Kh + j * d, *vj = Vh + j * d;
+  for (long c = 0; c < d; ++c) dKj[c] = dVj[c] = 0.0;
+  long i0 = causal ? j : 0;
+  for (long i = i0; i < N; ++i) {
+    const double *qi = Qh + i * d, *dOi = dOh + i * d;
+    double sij = scale * dot(qi, kj, d);
+    double p = exp(sij - Lh[i]);
+    double dp = dot(dOi, vj, d);
+    double ds = p * (dp - Dh[i]);
+    for (long c = 0; c < d; ++c) {
+      dKj[c] += ds * qi[c];
+      dVj[c] += p * dOi[c];
+    }
+  }
+  for (long c = 0; c < d; ++c) dKj[c] *= scale;
+}
+
+/* Pass 2: dQ for every query row. */
 static int pass_dq(const double *Q, const double *K, const double *V,
                    const double *dO, const double *L, const double *D, long BH,
                    long N, long d, int causal, double scale, double *dQ) {
@@ -142,21 +184,9 @@ static int pass_dq(const double *Q, const double *K, const double *V,
     for (long h = 0; h < BH; ++h) {
       for (long i = 0; i < N; ++i) {
         if (!srow) continue;
-        const double *Qh = Q + h * N * d, *Kh = K + h * N * d;
-        const double *Vh = V + h * N * d;
-        const double *dOi = dO + (h * N + i) * d;
-        long n = scores_row(Qh, Kh, i, N, d, causal, scale, srow);
-        double Li = L[h * N + i], Di = D[h * N + i];
-        double *dQi = dQ + (h * N + i) * d;
-        for (long c = 0; c < d; ++c) dQi[c] = 0.0;
-        for (long j = 0; j < n; ++j) {
-          double p = exp(srow[j] - Li);
-          double dp = dot(dOi, Vh + j * d, d);
-          double ds = p * (dp - Di);
-          const double *kj = Kh + j * d;
-          for (long c = 0; c < d; ++c) dQi[c] += ds * kj[c];
-        }
-        for (long c = 0; c < d; ++c) dQi[c] *= scale;
+        dq_row(Q + h * N * d, K + h * N * d, V + h * N * d, dO + h * N * d,
+               L + h * N, D + h * N, N, d, causal, scale, i, srow,
+               dQ + (h * N + i) * d);
       }
     }
     free(srow);
@@ -164,8 +194,7 @@ static int pass_dq(const double *Q, const double *K, const double *V,
   return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 
-/* Pass 3: dK_j = s * sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i for every key
- * row j.  Under the causal mask, key j is seen by query rows i >= j only. */
+/* Pass 3: dK and dV for every key row. */
 static int pass_dkdv(const double *Q, const double *K, const double *V,
                      const double *dO, const double *L, const double *D,
                      long BH, long N, long d, int causal, double scale,
@@ -173,24 +202,9 @@ static int pass_dkdv(const double *Q, const double *K, const double *V,
 #pragma omp parallel for collapse(2) schedule(dynamic, 16)
   for (long h = 0; h < BH; ++h) {
     for (long j = 0; j < N; ++j) {
-      const double *Qh = Q + h * N * d, *Kh = K + h * N * d;
-      const double *Vh = V + h * N * d, *dOh = dO + h * N * d;
-      const double *kj = Kh + j * d, *vj = Vh + j * d;
-      double *dKj = dK + (h * N + j) * d, *dVj = dV + (h * N + j) * d;
-      for (long c = 0; c < d; ++c) dKj[c] = dVj[c] = 0.0;
-      long i0 = causal ? j : 0;
-      for (long i = i0; i < N; ++i) {
-        const double *qi = Qh + i * d, *dOi = dOh + i * d;
-        double sij = scale * dot(qi, kj, d);
-        double p = exp(sij - L[h * N + i]);
-        double dp = dot(dOi, vj, d);
-        double ds = p * (dp - D[h * N + i]);
-        for (long c = 0; c < d; ++c) {
-          dKj[c] += ds * qi[c];
-          dVj[c] += p * dOi[c];
-        }
-      }
-      for (long c = 0; c < d; ++c) dKj[c] *= scale;
+      dkdv_row(Q + h * N * d, K + h * N * d, V + h * N * d, dO + h * N * d,
+               L + h * N, D + h * N, N, d, causal, scale, j,
+               dK + (h * N + j) * d, dV + (h * N + j) * d);
     }
   }
   return ORACLE_OK;
@@ -240,4 +254,63 @@ int oracle_max_threads(void) {
 #else
   return 1;
 #endif
+}
+
+/* Sampled rows of one head, for shapes too large to evaluate in full.
+ * Pass 1 runs over every query row (dK_j and dV_j need L_i and D_i of all
+ * rows); passes 2 and 3 run only over the requested query rows qrows[0..nq)
+ * and key rows krows[0..nk).  Outputs: O_rows, dQ_rows [nq][d], L_rows [nq],
+ * dK_rows, dV_rows [nk][d].  Q, K, V, dO are one head, [N][d]. */
+int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
+                          const double *dO, long N, long d, int causal,
+                          double scale, long nq, const long *qrows, long nk,
+                          const long *krows, double *O_rows, double *L_rows,
+                          double *dQ_rows, double *dK_rows, double *dV_rows,
+                          int nthreads) {
+  int st = check_args(Q, K, V, 1, N, d, scale);
+  if (st) return st;
+  if (nq < 0 || nk < 0 || (nq && (!qrows || !O_rows || !L_rows || !dQ_rows)) ||
+      (nk && (!krows || !dK_rows || !dV_rows)) || !dO)
+    return ORACLE_ERR_ARG;
+  for (long t = 0; t < nq; ++t)
+    if (qrows[t] < 0 || qrows[t] >= N) return ORACLE_ERR_ARG;
+  for (long t = 0; t < nk; ++t)
+    if (krows[t] < 0 || krows[t] >= N) return ORACLE_ERR_ARG;
+  if (N == 0) return ORACLE_OK;
+  set_threads(nthreads);
+  double *O = (double *)malloc(sizeof(double) * (size_t)(N * d));
+  double *L = (double *)malloc(sizeof(double) * (size_t)N);
+  double *D = (double *)malloc(sizeof(double) * (size_t)N);
+  if (!O || !L || !D) {
+    free(O); free(L); free(D);
+    return ORACLE_ERR_NOMEM;
+  }
+  st = pass_forward(Q, K, V, dO, 1, N, d, causal, scale, O, L, D);
+  if (!st) {
+    int failed = 0;
+#pragma omp parallel
+    {
+      double *srow = (double *)malloc(sizeof(double) * (size_t)N);
+      if (!srow) {
+#pragma omp atomic write
+        failed = 1;
+      }
+#pragma omp for schedule(dynamic, 1)
+      for (long t = 0; t < nq; ++t) {
+        if (!srow) continue;
+        long i = qrows[t];
+        memcpy(O_rows + t * d, O + i * d, sizeof(double) * (size_t)d);
+        L_rows[t] = L[i];
+        dq_row(Q, K, V, dO, L, D, N, d, causal, scale, i, srow, dQ_rows + t * d);
+      }
+#pragma omp for schedule(dynamic, 1)
+      for (long t = 0; t < nk; ++t)
+        dkdv_row(Q, K, V, dO, L, D, N, d, causal, scale, krows[t], dK_rows + t * d,
+                 dV_rows + t * d);
+      free(srow);
+    }
+    if (failed) st = ORACLE_ERR_NOMEM;
+  }
+  free(O); free(L); free(D);
+  return st;
 }

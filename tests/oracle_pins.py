@@ -288,6 +288,26 @@ def pin_torch_fp64(lib):
             _close(out["dV"], tv.grad.numpy(), 1e-10, what="torch dV")
 
 
+
+
+def pin_row_sampler_matches_full(lib):
+    """The row sampler evaluates the same definition as the full oracle: its
+    rows equal the full result's rows bit for bit (same arithmetic order)."""
+    rng = np.random.default_rng(19)
+    for causal in (False, True):
+        N, d = 57, 6
+        q, k, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(4))
+        full = _fb(lib, q, k, v, do, causal, 0.35)
+        qr, kr = [0, 5, 56, 31], [56, 0, 13]
+        rows = oracle.attention_head_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, 0.35,
+                                          qr, kr, lib=lib)
+        for name in ("O", "dQ"):
+            assert np.array_equal(rows[name], full[name][0, 0][qr]), name
+        assert np.array_equal(rows["L"], full["L"][0, 0][qr])
+        for name in ("dK", "dV"):
+            assert np.array_equal(rows[name], full[name][0, 0][kr]), name
+
+
 ALL_PINS = [
     pin_finite_differences,
     pin_single_key,
@@ -298,4 +318,5 @@ ALL_PINS = [
     pin_permutation,
     pin_brute_force,
     pin_torch_fp64,
+    pin_row_sampler_matches_full,
 ]

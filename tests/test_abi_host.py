@@ -1,0 +1,133 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+function include/attn.h declares, and validates arguments on the host
+(documented statuses, nothing launched).  CPU only."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_backward_pass_attn_gb300 import binding as ab
+from attention_backward_pass_attn_gb300 import build as abuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    abuild.build()
+    return ab.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size",
+                     "attn_last_device_error", "attn_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), "missing export %s" % name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_no_undeclared_attn_exports(lib):
+    # every binding signature corresponds to a declaration
+    names = set(declared_functions())
+    for name in ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
+                 "attn_bwd_dq_convert", "attn_device_error_word", "attn_watchdog_selftest",
+                 "attn_version"):
+        assert name in names
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        assert lib.attn_status_string(st)
+    assert lib.attn_status_string(99) == b"unknown status"
+    assert lib.attn_version() >= 100
+
+
+def test_workspace_size(lib):
+    # D and L2: BH*Npad fp32 each; acc: BH*Npad*d fp32; each section 256-aligned
+    def expect(B, H, N, d):
+        npad = (N + 127) // 128 * 128
+        r = lambda x: (x + 255) // 256 * 256
+        return 2 * r(4 * B * H * npad) + r(4 * B * H * npad * d)
+    for args in ((1, 2, 128, 64), (2, 16, 2048, 64), (1, 3, 129, 128), (4, 16, 8192, 128)):
+        assert lib.attn_bwd_workspace_size(*args) == expect(*args)
+    assert lib.attn_bwd_workspace_size(0, 2, 128, 64) == 0
+    assert lib.attn_bwd_workspace_size(1, 2, 0, 64) == 0
+    assert lib.attn_bwd_workspace_size(1, 2, 128, 96) == 0
+    assert lib.attn_bwd_workspace_size(-1, 2, 128, 64) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced
+
+
+def fwd(lib, Q=FAKE, K=FAKE, V=FAKE, O=FAKE, L=FAKE, B=1, H=1, N=128, d=64, causal=0, scale=0.125):
+    return lib.attn_fwd(Q, K, V, O, L, B, H, N, d, causal, scale, None)
+
+
+def bwd(lib, ptr=FAKE, B=1, H=1, N=128, d=64, causal=0, scale=0.125, ws=FAKE, wsb=None):
+    if wsb is None:
+        wsb = lib.attn_bwd_workspace_size(max(B, 0), max(H, 0), max(N, 0), d)
+    return lib.attn_bwd(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, B, H, N, d, causal, scale,
+                        ws, wsb, None)
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, Q=None) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, L=None) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, V=FAKE + 8) == ab.ATTN_ERR_INVALID_ARG       # misaligned
+    assert fwd(lib, B=-1) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, N=-5) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, d=96) == ab.ATTN_ERR_UNSUPPORTED
+    assert fwd(lib, d=256) == ab.ATTN_ERR_UNSUPPORTED
+    assert fwd(lib, causal=2) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, scale=0.0) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, scale=-1.0) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, scale=float("nan")) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, scale=float("inf")) == ab.ATTN_ERR_INVALID_ARG
+    assert fwd(lib, B=1 << 20, H=1 << 12) == ab.ATTN_ERR_UNSUPPORTED  # rows beyond 31 bits
+    # empty problems are valid and launch nothing, even with null pointers
+    assert fwd(lib, Q=None, K=None, V=None, O=None, L=None, N=0) == ab.ATTN_OK
+    assert fwd(lib, Q=None, K=None, V=None, O=None, L=None, B=0) == ab.ATTN_OK
+
+
+def test_bwd_validation(lib):
+    assert bwd(lib, ptr=None) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd(lib, d=32) == ab.ATTN_ERR_UNSUPPORTED
+    assert bwd(lib, H=-2) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd(lib, scale=0.0) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd(lib, ws=None) == ab.ATTN_ERR_WORKSPACE
+    assert bwd(lib, ws=FAKE + 16) == ab.ATTN_ERR_WORKSPACE               # not 256-aligned
+    need = lib.attn_bwd_workspace_size(1, 1, 128, 64)
+    assert bwd(lib, wsb=need - 1) == ab.ATTN_ERR_WORKSPACE
+    assert bwd(lib, ptr=None, ws=None, wsb=0, N=0) == ab.ATTN_OK
+    # the three steps validate the same way
+    assert lib.attn_bwd_preprocess(FAKE, FAKE, None, 1, 1, 128, 64, FAKE, need, None) == \
+        ab.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_preprocess(FAKE, FAKE, FAKE, 1, 1, 128, 64, FAKE, 0, None) == \
+        ab.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd_main(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 1, -0.5,
+                             FAKE, need, None) == ab.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_dq_convert(None, 1, 1, 128, 64, 0.125, FAKE, need, None) == \
+        ab.ATTN_ERR_INVALID_ARG
+    assert lib.attn_watchdog_selftest(10, None) == ab.ATTN_ERR_INVALID_ARG
+
+
+def test_binding_checks_tensors():
+    import torch
+
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ab.attn_fwd(q, q, q, causal=False)  # CPU tensors are rejected, nothing falls back

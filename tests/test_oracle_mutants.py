@@ -19,7 +19,7 @@ MUTANTS = {
     "dq_missing_scale": ("for (long c = 0; c < d; ++c) dQi[c] *= scale;", ""),
     "dk_missing_scale": ("for (long c = 0; c < d; ++c) dKj[c] *= scale;", ""),
     "ds_sign_flip_in_dq": ("double ds = p * (dp - Di);", "double ds = p * (dp + Di);"),
-    "ds_drops_D_in_dkdv": ("double ds = p * (dp - D[h * N + i]);", "double ds = p * dp;"),
+    "ds_drops_D_in_dkdv": ("double ds = p * (dp - Dh[i]);", "double ds = p * dp;"),
     "lse_without_log_sum": ("double Li = m + log(l);", "double Li = m;"),
     "dv_uses_ds": ("dVj[c] += p * dOi[c];", "dVj[c] += ds * dOi[c];"),
     "dkdv_ignores_causal": ("long i0 = causal ? j : 0;", "long i0 = 0;"),
