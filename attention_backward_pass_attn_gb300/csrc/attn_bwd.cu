@@ -77,12 +77,10 @@ struct Layout {
   static constexpr uint32_t kColDP = 2 * HD + 128;
 };
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int k) {
-  return make_sdesc_sw128(tile + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int k) {
-  return make_sdesc_sw128(tile + k * 2048, 16384, 1024);
-}
+// Descriptor conventions (128-byte swizzle, tiles of 128 rows in 64-column
+// blocks of 16 KB): a K-major operand advances 32 bytes per 16-element k-step
+// within a block and 16 KB across blocks; an MN-major operand advances 2 KB
+// (16 rows) per k-step, its MN extent spanning blocks 16 KB apart (LBO).
 
 template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -152,88 +150,125 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform operands); one lane issues.
+    if (elect_one()) {
       mbar_arrive_expect_tx(bar(kBarKV), 2 * Ly::kTileBytes);
+#pragma unroll
       for (int cb = 0; cb < HD / 64; ++cb) {
         tma_load_3d(sbase + Ly::kK + cb * 16384, &tmK, bar(kBarKV), cb * 64, jt * 128, bh);
         tma_load_3d(sbase + Ly::kV + cb * 16384, &tmV, bar(kBarKV), cb * 64, jt * 128, bh);
       }
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1, n = it >> 1, qt = it0 + it;
-        if (it >= 2 && !mbar_wait(bar(kBarQEmpty + s), (n - 1) & 1, ctx, 0x210)) break;
+    }
+    __syncwarp();
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1, n = it >> 1, qt = it0 + it;
+      if (it >= 2 && !mbar_wait_warp(bar(kBarQEmpty + s), (n - 1) & 1, ctx, 0x210)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar(kBarQFull + s), Ly::kTileBytes + 1024);
+#pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kQ + s * Ly::kTileBytes + cb * 16384, &tmQ, bar(kBarQFull + s),
                       cb * 64, qt * 128, bh);
         const size_t vo = size_t(bh) * Npad + size_t(qt) * 128;
         bulk_load(sbase + Ly::kVec + s * 1024, L2ws + vo, 512, bar(kBarQFull + s));
         bulk_load(sbase + Ly::kVec + s * 1024 + 512, Dws + vo, 512, bar(kBarQFull + s));
-        if (it >= 2 && !mbar_wait(bar(kBarDOEmpty + s), (n - 1) & 1, ctx, 0x211)) break;
+      }
+      __syncwarp();
+      if (it >= 2 && !mbar_wait_warp(bar(kBarDOEmpty + s), (n - 1) & 1, ctx, 0x211)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar(kBarDOFull + s), Ly::kTileBytes);
+#pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kDO + s * Ly::kTileBytes + cb * 16384, &tmdO,
                       bar(kBarDOFull + s), cb * 64, qt * 128, bh);
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
-      constexpr uint32_t kIdV = make_idesc_bf16(128, HD, 0, 1);    // dV, dK
-      constexpr uint32_t kIdQ = make_idesc_bf16(128, HD, 1, 1);    // dQ = dS K
-      const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV, sDS = sbase + Ly::kDS;
-      const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
-      const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
-      bool ok = mbar_wait(bar(kBarKV), 0, ctx, 0x220);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it & 1, ph = (it >> 1) & 1;
-        const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
-        const uint32_t sDO = sbase + Ly::kDO + s * Ly::kTileBytes;
-        // S^T = K Q^T
-        if (!(ok = mbar_wait(bar(kBarQFull + s), ph, ctx, 0x221))) break;
-        tc_fence_after();
+    // The whole warp runs the loop and waits; one elected lane issues.  Every
+    // descriptor is a per-tile base plus a compile-time k-step offset.
+    constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+    constexpr uint32_t kIdV = make_idesc_bf16(128, HD, 0, 1);    // dV, dK
+    constexpr uint32_t kIdQ = make_idesc_bf16(128, HD, 1, 1);    // dQ = dS K
+    const uint64_t dK_k = make_sdesc_sw128(sbase + Ly::kK, 16, 1024);        // K, K-major
+    const uint64_t dK_mn = make_sdesc_sw128(sbase + Ly::kK, 16384, 1024);    // K, MN-major
+    const uint64_t dV_k = make_sdesc_sw128(sbase + Ly::kV, 16, 1024);
+    const uint64_t dS_k = make_sdesc_sw128(sbase + Ly::kDS, 16, 1024);       // dS^T, K-major
+    const uint64_t dS_mn = make_sdesc_sw128(sbase + Ly::kDS, 16384, 1024);   // dS, MN-major
+    const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
+    const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
+    bool ok = mbar_wait_warp(bar(kBarKV), 0, ctx, 0x220);
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int s = it & 1, ph = (it >> 1) & 1;
+      const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
+      const uint32_t sDO = sbase + Ly::kDO + s * Ly::kTileBytes;
+      const uint64_t dQ_k = make_sdesc_sw128(sQ, 16, 1024), dQ_mn = make_sdesc_sw128(sQ, 16384, 1024);
+      const uint64_t dO_k = make_sdesc_sw128(sDO, 16, 1024), dO_mn = make_sdesc_sw128(sDO, 16384, 1024);
+      const uint32_t acc0 = it > 0 ? 1u : 0u;
+      // S^T = K Q^T
+      if (!(ok = mbar_wait_warp(bar(kBarQFull + s), ph, ctx, 0x221))) break;
+      tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tS, kmajor_desc(sK, k), kmajor_desc(sQ, k), kIdS, k > 0);
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tS, sdesc_add(dK_k, off), sdesc_add(dQ_k, off), kIdS, k > 0 ? 1u : 0u);
+        }
         tc_commit(bar(kBarSFull));
-        // dP^T = V dO^T  (its columns held dQ of the previous tile: wait for the drain)
-        if (!(ok = mbar_wait(bar(kBarDOFull + s), ph, ctx, 0x222))) break;
-        if (it > 0 && !(ok = mbar_wait(bar(kBarDQFree), (it - 1) & 1, ctx, 0x223))) break;
-        tc_fence_after();
+      }
+      __syncwarp();
+      // dP^T = V dO^T  (its columns held dQ of the previous tile: wait for the drain)
+      if (!(ok = mbar_wait_warp(bar(kBarDOFull + s), ph, ctx, 0x222))) break;
+      if (it > 0 && !(ok = mbar_wait_warp(bar(kBarDQFree), (it - 1) & 1, ctx, 0x223))) break;
+      tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(tDP, kmajor_desc(sV, k), kmajor_desc(sDO, k), kIdS, k > 0);
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tDP, sdesc_add(dV_k, off), sdesc_add(dO_k, off), kIdS, k > 0 ? 1u : 0u);
+        }
         tc_commit(bar(kBarDPFull));
-        // dV += P^T dO, P^T read from tensor memory: query block k/4 was packed by
-        // the softmax warps of that half into its own first 32 columns.
-        if (!(ok = mbar_wait(bar(kBarPReady), it & 1, ctx, 0x224))) break;
-        tc_fence_after();
+      }
+      __syncwarp();
+      // dV += P^T dO, P^T read from tensor memory: query block k/4 was packed by
+      // the softmax warps of that half into its own first 32 columns.
+      if (!(ok = mbar_wait_warp(bar(kBarPReady), it & 1, ctx, 0x224))) break;
+      tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tDV, tS + 64 * (k >> 2) + 8 * (k & 3), mnmajor_desc(sDO, k), kIdV,
-                 (it > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tDV, tS + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(dO_mn, k * 2048), kIdV,
+                 k > 0 ? 1u : acc0);
         tc_commit(bar(kBarDOEmpty + s));
-        // dK += dS^T Q, then dQ_i = dS K into the dP^T columns
-        if (!(ok = mbar_wait(bar(kBarDSReady), it & 1, ctx, 0x225))) break;
-        tc_fence_after();
+      }
+      __syncwarp();
+      // dK += dS^T Q, then dQ_i = dS K into the dP^T columns
+      if (!(ok = mbar_wait_warp(bar(kBarDSReady), it & 1, ctx, 0x225))) break;
+      tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tDK, kmajor_desc(sDS, k), mnmajor_desc(sQ, k), kIdV, (it > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tDK, sdesc_add(dS_k, off), sdesc_add(dQ_mn, k * 2048), kIdV, k > 0 ? 1u : acc0);
+        }
         tc_commit(bar(kBarQEmpty + s));
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tDP, mnmajor_desc(sDS, k), mnmajor_desc(sK, k), kIdQ, k > 0);
+          mma_ss(tDP, sdesc_add(dS_mn, k * 2048), sdesc_add(dK_mn, k * 2048), kIdQ, k > 0 ? 1u : 0u);
         tc_commit(bar(kBarDQFull));
         tc_commit(bar(kBarDSFree));
       }
+      __syncwarp();
+    }
+    if (elect_one()) {
       tc_commit(bar(kBarAccFull));
       tc_commit(bar(kBarDrain));
-      volatile int never = 0;
-      const WaitCtx own{&never, err, kWaitLimitNs};
-      mbar_wait(bar(kBarDrain), 0, own, 0x22F);
     }
     __syncwarp();
+    volatile int never = 0;  // this wait ignores the CTA abort flag
+    const WaitCtx own{&never, err, kWaitLimitNs};
+    mbar_wait_warp(bar(kBarDrain), 0, own, 0x22F);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / dS
     const int h = (warp - 4) >> 2;       // query half: columns 64h .. 64h+63

@@ -67,16 +67,10 @@ struct Layout {
   static constexpr uint32_t kColS = 2 * HD;      // + tile * 128
 };
 
-// K-major operand, 128-byte swizzle: K-step k (16 bf16) of a tile whose rows
-// hold HD contiguous values split in 64-column blocks of 16 KB.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int k) {
-  return make_sdesc_sw128(tile + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-}
-// MN-major operand: K-step k covers tile rows 16k..16k+15; the MN extent runs
-// along the row, across 64-column blocks 16 KB apart.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int k) {
-  return make_sdesc_sw128(tile + k * 2048, 16384, 1024);
-}
+// Descriptor conventions (128-byte swizzle, tiles of 128 rows in 64-column
+// blocks of 16 KB): a K-major operand advances 32 bytes per 16-element k-step
+// within a block and 16 KB across blocks; an MN-major operand advances 2 KB
+// (16 rows) per k-step, its MN extent spanning blocks 16 KB apart (LBO).
 
 template <int HD, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -139,87 +133,114 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform operands); one lane issues.
+    if (elect_one()) {
       mbar_arrive_expect_tx(bar(kBarQFull), (has_b ? 2 : 1) * Ly::kTileBytes);
       for (int t = 0; t < (has_b ? 2 : 1); ++t)
+#pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kQ + t * Ly::kTileBytes + cb * 16384, &tmQ, bar(kBarQFull),
                       cb * 64, (qt_a + t) * 128, bh);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % kStages, n = j / kStages;
-        if (j >= kStages && !mbar_wait(bar(kBarKEmpty + s), (n - 1) & 1, ctx, 0x110)) break;
+    }
+    __syncwarp();
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j % kStages, n = j / kStages;
+      if (j >= kStages && !mbar_wait_warp(bar(kBarKEmpty + s), (n - 1) & 1, ctx, 0x110)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar(kBarKFull + s), Ly::kTileBytes);
+#pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kK + s * Ly::kTileBytes + cb * 16384, &tmK,
                       bar(kBarKFull + s), cb * 64, j * 128, bh);
-        if (j >= kStages && !mbar_wait(bar(kBarVEmpty + s), (n - 1) & 1, ctx, 0x111)) break;
+      }
+      __syncwarp();
+      if (j >= kStages && !mbar_wait_warp(bar(kBarVEmpty + s), (n - 1) & 1, ctx, 0x111)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(bar(kBarVFull + s), Ly::kTileBytes);
+#pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kV + s * Ly::kTileBytes + cb * 16384, &tmV,
                       bar(kBarVFull + s), cb * 64, j * 128, bh);
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);  // S = Q K^T
-      constexpr uint32_t kIdO = make_idesc_bf16(128, HD, 0, 1);   // O += P V
-      auto issue_s = [&](int t, int stage) {
-        const uint32_t qa = sbase + Ly::kQ + t * Ly::kTileBytes;
-        const uint32_t ka = sbase + Ly::kK + stage * Ly::kTileBytes;
-        const uint32_t d = tbase + Ly::kColS + 128 * t;
+    // The whole warp runs the loop and waits; one elected lane issues.  Every
+    // descriptor is a per-tile base plus a compile-time k-step offset.
+    constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);  // S = Q K^T
+    constexpr uint32_t kIdO = make_idesc_bf16(128, HD, 0, 1);   // O += P V
+    const uint64_t dQa = make_sdesc_sw128(sbase + Ly::kQ, 16, 1024);
+    const uint64_t dQb = make_sdesc_sw128(sbase + Ly::kQ + Ly::kTileBytes, 16, 1024);
+    auto issue_s = [&](int t, int stage) {  // elected lane only
+      const uint64_t dq = t == 0 ? dQa : dQb;
+      const uint64_t dk = make_sdesc_sw128(sbase + Ly::kK + stage * Ly::kTileBytes, 16, 1024);
+      const uint32_t d = tbase + Ly::kColS + 128 * t;
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          mma_ss(d, kmajor_desc(qa, k), kmajor_desc(ka, k), kIdS, k > 0);
-        tc_commit(bar(kBarSFull + t));
-      };
-      auto issue_pv = [&](int t, int stage, bool acc) {
-        const uint32_t va = sbase + Ly::kV + stage * Ly::kTileBytes;
-        const uint32_t d = tbase + Ly::kColO + HD * t;
-        const uint32_t p = tbase + Ly::kColS + 128 * t;
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+        mma_ss(d, sdesc_add(dq, off), sdesc_add(dk, off), kIdS, k > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(kBarSFull + t));
+    };
+    auto issue_pv = [&](int t, int stage, uint32_t acc) {  // elected lane only
+      const uint64_t dv = make_sdesc_sw128(sbase + Ly::kV + stage * Ly::kTileBytes, 16384, 1024);
+      const uint32_t d = tbase + Ly::kColO + HD * t;
+      const uint32_t p = tbase + Ly::kColS + 128 * t;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)  // 128 keys, 16 per step; P packed 2 per column
-          mma_ts(d, p + 8 * k, mnmajor_desc(va, k), kIdO, (acc || k > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(bar(kBarQFull), 0, ctx, 0x120) &&
-                mbar_wait(bar(kBarKFull), 0, ctx, 0x121);
-      if (ok) {
-        tc_fence_after();
+      for (int k = 0; k < 8; ++k)  // 128 keys, 16 per step; P packed 2 per column
+        mma_ts(d, p + 8 * k, sdesc_add(dv, k * 2048), kIdO, k > 0 ? 1u : acc);
+    };
+    bool ok = mbar_wait_warp(bar(kBarQFull), 0, ctx, 0x120) &&
+              mbar_wait_warp(bar(kBarKFull), 0, ctx, 0x121);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
         issue_s(0, 0);
         if (has_b) issue_s(1, 0);
         tc_commit(bar(kBarKEmpty));
-        for (int j = 0; j < n_kv && ok; ++j) {
-          const int s = j % kStages;
-          const bool next = j + 1 < n_kv;
-          const int s1 = (j + 1) % kStages, n1 = (j + 1) / kStages;
-          if (!(ok = mbar_wait(bar(kBarVFull + s), (j / kStages) & 1, ctx, 0x122))) break;
-          if (!(ok = mbar_wait(bar(kBarPReady + 0), j & 1, ctx, 0x123))) break;
+      }
+      __syncwarp();
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j % kStages;
+        const bool next = j + 1 < n_kv;
+        const int s1 = (j + 1) % kStages, n1 = (j + 1) / kStages;
+        const uint32_t acc = j > 0 ? 1u : 0u;
+        if (!(ok = mbar_wait_warp(bar(kBarVFull + s), (j / kStages) & 1, ctx, 0x122))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarPReady + 0), j & 1, ctx, 0x123))) break;
+        tc_fence_after();
+        if (elect_one()) issue_pv(0, s, acc);
+        __syncwarp();
+        if (next) {
+          if (!(ok = mbar_wait_warp(bar(kBarKFull + s1), n1 & 1, ctx, 0x124))) break;
           tc_fence_after();
-          issue_pv(0, s, j > 0);
-          if (next) {
-            if (!(ok = mbar_wait(bar(kBarKFull + s1), n1 & 1, ctx, 0x124))) break;
-            tc_fence_after();
-            issue_s(0, s1);
-          }
-          if (has_b) {
-            if (!(ok = mbar_wait(bar(kBarPReady + 1), j & 1, ctx, 0x125))) break;
-            tc_fence_after();
-            issue_pv(1, s, j > 0);
+          if (elect_one()) issue_s(0, s1);
+          __syncwarp();
+        }
+        if (has_b) {
+          if (!(ok = mbar_wait_warp(bar(kBarPReady + 1), j & 1, ctx, 0x125))) break;
+          tc_fence_after();
+          if (elect_one()) {
+            issue_pv(1, s, acc);
             if (next) issue_s(1, s1);
           }
+          __syncwarp();
+        }
+        if (elect_one()) {
           tc_commit(bar(kBarVEmpty + s));
           if (next) tc_commit(bar(kBarKEmpty + s1));
         }
-        tc_commit(bar(kBarOFull));
+        __syncwarp();
       }
-      // Wait until every MMA issued above has completed before teardown.
-      tc_commit(bar(kBarDrain));
-      volatile int never = 0;  // this wait ignores the CTA abort flag
-      const WaitCtx own{&never, err, kWaitLimitNs};
-      mbar_wait(bar(kBarDrain), 0, own, 0x12F);
+      if (elect_one()) tc_commit(bar(kBarOFull));
+      __syncwarp();
     }
+    // Wait until every MMA issued above has completed before teardown.
+    if (elect_one()) tc_commit(bar(kBarDrain));
     __syncwarp();
+    volatile int never = 0;  // this wait ignores the CTA abort flag
+    const WaitCtx own{&never, err, kWaitLimitNs};
+    mbar_wait_warp(bar(kBarDrain), 0, own, 0x12F);
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;  // 0 = tile A, 1 = tile B

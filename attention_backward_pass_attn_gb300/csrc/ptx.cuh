@@ -114,6 +114,17 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, ok);
 }
 
+// One lane of a converged warp gets true.  The MMA and TMA roles run their
+// loops on the whole warp (so addresses and descriptors stay warp-uniform)
+// and let the elected lane issue.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
@@ -219,6 +230,13 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
                                                      uint32_t sbo_bytes) {
   return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16) |
          (uint64_t((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Advance a shared-memory descriptor by a byte offset (a multiple of 16 that
+// keeps the address inside the 14-bit start field): descriptors for the
+// k-steps of one tile are one base plus compile-time offsets.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_offset) {
+  return desc + uint64_t(byte_offset >> 4);
 }
 
 // ---------------------------------------------------------------------------

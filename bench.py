@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch: attn_fwd (O, L), then
+attn_bwd = preprocess (D) + fused main kernel (dK, dV, dQ accumulation) + dQ
+convert.  The headline metric is backward TFLOP/s: 10*B*H*N^2*d FLOPs
+(halved under the causal mask) divided by the device time of attn_bwd.
+
+Timing: W untimed warm-up steps, then exactly K timed steps; before every
+step a 512 MiB buffer is written to flush the 129 MB L2; each step is
+bracketed by CUDA events on the launching stream; a barrier and a device
+synchronisation bracket the timed region; with several ranks the time is the
+maximum over ranks.  nvidia-smi samples SM clocks and throttle reasons during
+the timed region.
+
+Legs reported on the one JSON line (rank 0):
+  value       backward TFLOP/s, inputs resident in HBM
+  e2e         the same metric through the public API with pinned HOST
+              buffers: host->device inputs, forward, backward, device->host
+              gradients, all inside the timed step
+  roofline    the backward main kernel (tensor-bound) against the measured
+              dense bf16 peak
+  cpu_baseline the fp64 oracle on the host cores, on a bounded sample
+  d128_backward  the three d = 128 workloads (N >= 4096), main-kernel TF/s
+
+--impl reference times the fp64 CPU oracle (the only reference this project
+has) on the same workload, metric and unit.
+
+Multi-GPU (torchrun, one rank per GPU): heads are independent, so every rank
+runs its own replica of the workload with no collective on the data path
+(weak scaling); value = all ranks' FLOPs / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "b2h16n2048d64_causal"
+D128 = ["b1h32n4096d128_causal", "b4h16n8192d128", "b1h16n16384d128_causal"]
+METRIC = "attention backward TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 peak"
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: a stored ncu traffic figure is only used if
+    the kernels have not changed since it was captured."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_backward_pass_attn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if still valid."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = table.get("%s@%s" % (kernel, workload))
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_ms: float, local_flops: float, group=None):
+    """(max time over ranks, total FLOPs over ranks): the slowest rank sets the
+    job time; every rank's work counts."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_ms, local_flops
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    f = torch.tensor([local_flops], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(f.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- our arm
+def time_workload(w, steps: int, warmup: int, flush, with_events=True):
+    """Run fwd + bwd `warmup + steps` times; returns per-step event times (ms)."""
+    import torch
+
+    from attention_backward_pass_attn_gb300 import binding as ab
+    from attention_backward_pass_attn_gb300.inputs import make_inputs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = ab.alloc_workspace(w.B, w.H, w.N, w.d, dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream)
+        e[1].record(stream)
+        ab.attn_bwd_preprocess(o, do, lse, ws, stream=stream)
+        e[2].record(stream)
+        ab.attn_bwd_main(q, k, v, do, dk, dv, w.causal, ws, scale=w.scale, stream=stream)
+        e[3].record(stream)
+        ab.attn_bwd_dq_convert(dq, ws, scale=w.scale, stream=stream)
+
+    rec = []
+    for i in range(warmup + steps):
+        flush()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        e[0].record(stream)
+        step()
+        e[4].record(stream)
+        if i >= warmup:
+            rec.append(e)
+    torch.cuda.synchronize()
+    st = ab.attn_last_device_error()
+    if st != ab.ATTN_OK:
+        raise RuntimeError("device error status %d during the benchmark" % st)
+    out = {"fwd": [], "prep": [], "main": [], "conv": [], "bwd": [], "step": []}
+    for e in rec:
+        t = [e[i].elapsed_time(e[i + 1]) for i in range(4)]
+        out["fwd"].append(t[0])
+        out["prep"].append(t[1])
+        out["main"].append(t[2])
+        out["conv"].append(t[3])
+        out["bwd"].append(t[1] + t[2] + t[3])
+        out["step"].append(sum(t))
+    return out
+
+
+def e2e_workload(w, steps: int, warmup: int, flush):
+    """The same step through the public API with pinned host buffers."""
+    import torch
+
+    from attention_backward_pass_attn_gb300 import binding as ab
+    from attention_backward_pass_attn_gb300.inputs import make_inputs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    host_in = [t.pin_memory() for t in make_inputs(w)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in host_in[:3]]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    o = torch.empty_like(dev_in[0])
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    grads = [torch.empty_like(dev_in[0]) for _ in range(3)]
+    ws = ab.alloc_workspace(w.B, w.H, w.N, w.d, dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(warmup + steps):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        q, k, v, do = dev_in
+        ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream)
+        ab.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=grads[0], dk=grads[1],
+                    dv=grads[2], workspace=ws, stream=stream)
+        for d, h in zip(grads, host_out):
+            h.copy_(d, non_blocking=True)
+        e1.record(stream)
+        if i >= warmup:
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in times]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w, min_seconds: float = 10.0):
+    """The fp64 oracle, as it stands, on the host cores: whole passes over the
+    workload's heads until at least `min_seconds` of CPU wall time."""
+    import oracle
+    from attention_backward_pass_attn_gb300.inputs import make_inputs
+
+    q, k, v, do = make_inputs(w)
+    lib = oracle.load()
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention_forward_backward(q, k, v, do, w.causal, w.scale, lib=lib)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= 50:
+            break
+    per_pass = el / passes
+    return {"value": w.bwd_flops() / per_pass / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.max_threads(lib), "kind": "oracle",
+            "sample": "%d full pass(es) of %s (all %d heads), fp64 fwd+bwd, %.1f s each; "
+                      "backward FLOPs / pass time" % (passes, w.name, w.heads, per_pass)}
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from attention_backward_pass_attn_gb300 import binding as ab
+    from attention_backward_pass_attn_gb300.inputs import WORKLOADS
+
+    ab.load_library()
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks["bf16_tflops"])
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    # warm-up outside the sampled window, then the timed region
+    time_workload(w, 0, max(args.warmup, 3), flush)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    res = time_workload(w, args.steps, 0, flush)
+    torch.cuda.synchronize()
+    barrier()
+    wall_s = time.perf_counter() - t_wall0
+    time.sleep(0.2)
+    clocks = sampler.stop()
+
+    bwd_ms_total = sum(res["bwd"])
+    step_ms_total = sum(res["step"])
+    bwd_max_ms, flops_all = aggregate(bwd_ms_total, w.bwd_flops() * args.steps)
+    step_max_ms, _ = aggregate(step_ms_total, 0.0)
+    value = flops_all / (bwd_max_ms * 1e-3) / 1e12
+
+    main_ms = statistics.mean(res["main"])
+    achieved = w.bwd_flops() / (main_ms * 1e-3) / 1e12
+
+    e2e_ms, h2d, d2h = e2e_workload(w, max(10, min(args.steps, 200)), 3, flush)
+    e2e_max, e2e_flops = aggregate(sum(e2e_ms), w.bwd_flops() * len(e2e_ms))
+    e2e_value = e2e_flops / (e2e_max * 1e-3) / 1e12
+
+    extra = None
+    if not args.no_extra:
+        extra = {}
+        for name in D128:
+            r = time_workload(WORKLOADS[name], 10, 3, flush)
+            mm = statistics.median(r["main"])
+            extra[name] = {
+                "bwd_main_tflops": round(WORKLOADS[name].bwd_flops() / mm / 1e9, 1),
+                "bwd_main_frac": round(WORKLOADS[name].bwd_flops() / mm / 1e9 / peak_tf, 4),
+                "bwd_total_tflops": round(WORKLOADS[name].bwd_flops()
+                                          / statistics.median(r["bwd"]) / 1e9, 1),
+                "fwd_tflops": round(WORKLOADS[name].fwd_flops()
+                                    / statistics.median(r["fwd"]) / 1e9, 1),
+                "main_ms_median": round(mm, 4),
+            }
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_max_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 inputs (no dataset)",
+        "config": {
+            "workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "scale": "1/sqrt(d)", "l2": "flushed before every step (512 MiB write)",
+            "timing": "CUDA events per step on the launching stream; value = backward FLOPs "
+                      "(10*B*H*N^2*d, halved causal) / attn_bwd device time",
+            "parallelism": "replicas (independent heads), no collective on the data path",
+        },
+        "fwd_tflops": round(w.fwd_flops() / statistics.mean(res["fwd"]) / 1e9, 2),
+        "bwd_ms": round(bwd_ms_total / args.steps, 5),
+        "fwd_ms": round(sum(res["fwd"]) / args.steps, 5),
+        "wall_s_timed_region": round(wall_s, 3),
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(statistics.mean(e2e_ms), 5),
+                "what": "pinned host inputs -> device, attn_fwd, attn_bwd, gradients -> host; "
+                        "backward FLOPs / whole step time"},
+        "roofline": {
+            "kernel": "attn_bwd_main_kernel", "bound": "tensor",
+            "achieved": round(achieved, 2), "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": round(achieved / peak_tf, 4),
+            "traffic": stored_traffic("attn_bwd_main_kernel", w.name),
+            "peak_source": "%s bf16_tflops (burst; the kernel is timed in a short step)"
+                           % ("of measured" if peak_src == "measured" else "of fallback"),
+            "flops_per_launch": w.bwd_flops(),
+            "avg_launch_ms": round(main_ms, 5),
+        },
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if extra is not None:
+        line["d128_backward"] = extra
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    return line
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm.  Each step evaluates a bounded
+    sample of the same workload, sized by a calibration run so that the whole
+    warm-up + timed run stays within about three minutes: whole heads when a
+    head fits the per-step budget, otherwise evenly spaced query rows of the
+    first head (their O, L and dQ)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    from attention_backward_pass_attn_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    q, k, v, do = make_inputs(w)
+    flat = [t.reshape(w.B * w.H, 1, w.N, w.d) for t in (q, k, v, do)]
+    lib = oracle.load()
+    per_step_budget = 180.0 / max(1, args.steps + args.warmup)
+    t0 = time.perf_counter()
+    oracle.attention_forward_backward(*(t[:1] for t in flat), w.causal, w.scale, lib=lib)
+    t_head = time.perf_counter() - t0
+    if t_head <= per_step_budget:
+        heads = int(max(1, min(w.heads, per_step_budget // t_head)))
+        sample = [t[:heads] for t in flat]
+        sample_flops = w.bwd_flops() * heads / w.heads
+
+        def step():
+            oracle.attention_forward_backward(*sample, w.causal, w.scale, lib=lib)
+
+        desc = "first %d of %d heads of %s per step (fp64 fwd+bwd)" % (heads, w.heads, w.name)
+    else:
+        rows = int(max(1, min(w.N, w.N * per_step_budget / t_head)))
+        idx = np.unique(np.linspace(0, w.N - 1, rows).astype(np.int64))
+        h0 = [t[0, 0] for t in flat]
+        sample_flops = w.bwd_flops() / w.heads * len(idx) / w.N
+
+        def step():
+            oracle.attention_head_rows(*h0, w.causal, w.scale, idx, [], lib=lib)
+
+        desc = ("%d evenly spaced query rows of head 0 of %s per step (fp64 O, L, dQ); "
+                "FLOPs counted pro rata" % (len(idx), w.name))
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = sample_flops * args.steps / el / 1e12
+    cores = oracle.max_threads(lib)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) bf16 inputs (no dataset)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=HEADLINE)
+    p.add_argument("--no-extra", action="store_true", help="skip the d=128 workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        p.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    try:
+        import torch.distributed as dist
+
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

@@ -86,6 +86,28 @@ static void set_threads(int nthreads) {
 #endif
 }
 
+/* L_i, O_i and (when dOh is given) D_i = <dO_i, O_i> for one query row i of
+ * one head. */
+static void fwd_row(const double *Qh, const double *Kh, const double *Vh,
+                    const double *dOh, long N, long d, int causal, double scale,
+                    long i, double *srow, double *Li_out, double *Oi,
+                    double *Di_out) {
+  long n = scores_row(Qh, Kh, i, N, d, causal, scale, srow);
+  double m = -INFINITY;
+  for (long j = 0; j < n; ++j) m = srow[j] > m ? srow[j] : m;
+  double l = 0.0;
+  for (long j = 0; j < n; ++j) l += exp(srow[j] - m);
+  double Li = m + log(l);
+  *Li_out = Li;
+  for (long c = 0; c < d; ++c) Oi[c] = 0.0;
+  for (long j = 0; j < n; ++j) {
+    double p = exp(srow[j] - Li);
+    const double *vj = Vh + j * d;
+    for (long c = 0; c < d; ++c) Oi[c] += p * vj[c];
+  }
+  if (dOh && Di_out) *Di_out = dot(dOh + i * d, Oi, d);
+}
+
 /* Pass 1: L, O and D for every query row. */
 static int pass_forward(const double *Q, const double *K, const double *V,
                         const double *dO, long BH, long N, long d, int causal,
@@ -102,23 +124,9 @@ static int pass_forward(const double *Q, const double *K, const double *V,
     for (long h = 0; h < BH; ++h) {
       for (long i = 0; i < N; ++i) {
         if (!srow) continue;
-        const double *Qh = Q + h * N * d, *Kh = K + h * N * d;
-        const double *Vh = V + h * N * d;
-        long n = scores_row(Qh, Kh, i, N, d, causal, scale, srow);
-        double m = -INFINITY;
-        for (long j = 0; j < n; ++j) m = srow[j] > m ? srow[j] : m;
-        double l = 0.0;
-        for (long j = 0; j < n; ++j) l += exp(srow[j] - m);
-        double Li = m + log(l);
-        L[h * N + i] = Li;
-        double *Oi = O + (h * N + i) * d;
-        for (long c = 0; c < d; ++c) Oi[c] = 0.0;
-        for (long j = 0; j < n; ++j) {
-          double p = exp(srow[j] - Li);
-          const double *vj = Vh + j * d;
-          for (long c = 0; c < d; ++c) Oi[c] += p * vj[c];
-        }
-        if (D) D[h * N + i] = dot(dO + (h * N + i) * d, Oi, d);
+        fwd_row(Q + h * N * d, K + h * N * d, V + h * N * d,
+                dO ? dO + h * N * d : NULL, N, d, causal, scale, i, srow,
+                L + h * N + i, O + (h * N + i) * d, D ? D + h * N + i : NULL);
       }
     }
     free(srow);
@@ -128,12 +136,10 @@ static int pass_forward(const double *Q, const double *K, const double *V,
 
 /* dQ_i = s * sum_j P_ij (dP_ij - D_i) k_j for one query row i of one head. */
 static void dq_row(const double *Qh, const double *Kh, const double *Vh,
-                   const double *dOh, const double *Lh, const double *Dh, long N,
-                   long d, int causal, double scale, long i, double *srow,
-                   double *dQi) {
+                   const double *dOh, double Li, double Di, long N, long d,
+                   int causal, double scale, long i, double *srow, double *dQi) {
   const double *dOi = dOh + i * d;
   long n = scores_row(Qh, Kh, i, N, d, causal, scale, srow);
-  double Li = Lh[i], Di = Dh[i];
   for (long c = 0; c < d; ++c) dQi[c] = 0.0;
   for (long j = 0; j < n; ++j) {
     double p = exp(srow[j] - Li);
@@ -185,7 +191,7 @@ static int pass_dq(const double *Q, const double *K, const double *V,
       for (long i = 0; i < N; ++i) {
         if (!srow) continue;
         dq_row(Q + h * N * d, K + h * N * d, V + h * N * d, dO + h * N * d,
-               L + h * N, D + h * N, N, d, causal, scale, i, srow,
+               L[h * N + i], D[h * N + i], N, d, causal, scale, i, srow,
                dQ + (h * N + i) * d);
       }
     }
@@ -278,6 +284,29 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
     if (krows[t] < 0 || krows[t] >= N) return ORACLE_ERR_ARG;
   if (N == 0) return ORACLE_OK;
   set_threads(nthreads);
+  if (nk == 0) {
+    /* Query rows only: O_i, L_i, D_i and dQ_i depend on row i alone. */
+    int failed = 0;
+#pragma omp parallel
+    {
+      double *srow = (double *)malloc(sizeof(double) * (size_t)N);
+      double Li = 0.0, Di = 0.0;
+      if (!srow) {
+#pragma omp atomic write
+        failed = 1;
+      }
+#pragma omp for schedule(dynamic, 1)
+      for (long t = 0; t < nq; ++t) {
+        if (!srow) continue;
+        long i = qrows[t];
+        fwd_row(Q, K, V, dO, N, d, causal, scale, i, srow, &Li, O_rows + t * d, &Di);
+        L_rows[t] = Li;
+        dq_row(Q, K, V, dO, Li, Di, N, d, causal, scale, i, srow, dQ_rows + t * d);
+      }
+      free(srow);
+    }
+    return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+  }
   double *O = (double *)malloc(sizeof(double) * (size_t)(N * d));
   double *L = (double *)malloc(sizeof(double) * (size_t)N);
   double *D = (double *)malloc(sizeof(double) * (size_t)N);
@@ -301,7 +330,7 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
         long i = qrows[t];
         memcpy(O_rows + t * d, O + i * d, sizeof(double) * (size_t)d);
         L_rows[t] = L[i];
-        dq_row(Q, K, V, dO, L, D, N, d, causal, scale, i, srow, dQ_rows + t * d);
+        dq_row(Q, K, V, dO, L[i], D[i], N, d, causal, scale, i, srow, dQ_rows + t * d);
       }
 #pragma omp for schedule(dynamic, 1)
       for (long t = 0; t < nk; ++t)

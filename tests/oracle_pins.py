@@ -306,6 +306,12 @@ def pin_row_sampler_matches_full(lib):
         assert np.array_equal(rows["L"], full["L"][0, 0][qr])
         for name in ("dK", "dV"):
             assert np.array_equal(rows[name], full[name][0, 0][kr]), name
+        # query rows only (no key rows): each row is evaluated on its own
+        qonly = oracle.attention_head_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, 0.35,
+                                           qr, [], lib=lib)
+        for name in ("O", "dQ"):
+            assert np.array_equal(qonly[name], full[name][0, 0][qr]), name
+        assert np.array_equal(qonly["L"], full["L"][0, 0][qr])
 
 
 ALL_PINS = [

@@ -25,8 +25,8 @@ MUTANTS = {
     "dkdv_ignores_causal": ("long i0 = causal ? j : 0;", "long i0 = 0;"),
     "causal_excludes_diagonal": ("return causal ? i + 1 : N;", "return causal ? (i > 0 ? i : 1) : N;"),
     "dk_uses_k_not_q": ("dKj[c] += ds * qi[c];", "dKj[c] += ds * kj[c];"),
-    "D_uses_dq_row": ("if (D) D[h * N + i] = dot(dO + (h * N + i) * d, Oi, d);",
-                      "if (D) D[h * N + i] = dot(dO + (h * N + (N - 1 - i)) * d, Oi, d);"),
+    "D_uses_wrong_row": ("if (dOh && Di_out) *Di_out = dot(dOh + i * d, Oi, d);",
+                         "if (dOh && Di_out) *Di_out = dot(dOh + (N - 1 - i) * d, Oi, d);"),
 }
 
 
