@@ -124,6 +124,20 @@ int make_tile_map(CUtensorMap* map, const void* ptr, const Shape& s) {
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+int make_acc_map(CUtensorMap* map, const float* acc, const Shape& s) {
+  auto encode = encode_fn();
+  if (!encode) return -1;
+  const cuuint64_t dims[2] = {cuuint64_t(s.d), cuuint64_t(s.BH) * cuuint64_t(s.Npad)};
+  const cuuint64_t strides[1] = {cuuint64_t(s.d) * 4};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(acc), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -195,12 +209,13 @@ int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, v
   if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
   int* err = error_word_ptr();
   if (!err) return ATTN_ERR_CUDA;
-  CUtensorMap mq, mk, mv, mdo;
+  const Workspace ws = carve_workspace(workspace, s);
+  CUtensorMap mq, mk, mv, mdo, macc;
   if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s) ||
-      make_tile_map(&mdo, dO, s))
+      make_tile_map(&mdo, dO, s) || make_acc_map(&macc, ws.acc, s))
     return ATTN_ERR_CUDA;
-  return cuda_status(launch_bwd_main(mq, mk, mv, mdo, dK, dV, carve_workspace(workspace, s), s,
-                                     scale, err, (cudaStream_t)stream));
+  return cuda_status(launch_bwd_main(mq, mk, mv, mdo, macc, dK, dV, ws, s, scale, err,
+                                     (cudaStream_t)stream));
 }
 
 int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,

@@ -16,8 +16,9 @@
 //        dV  += P^T dO            (A operand read from tensor memory)
 //        dS^T = P^T o (dP^T - D)  softmax warps, bf16 into shared memory
 //        dK  += dS^T Q
-//        dQ_i = dS K              (tensor memory, then fp32 vector reductions
-//                                  into the accumulator)
+//        dQ_i = dS K              (tensor memory, then staged through shared
+//                                  memory and added into the fp32
+//                                  accumulator by TMA reduce-add)
 //     dK and dV stay in tensor memory for the whole loop and are written once.
 //  3. attn_bwd_dq_convert_kernel: dQ = bf16(s * accumulator) (HBM-bound).
 //
@@ -26,7 +27,14 @@
 // S^T/dP^T (one key row = one tensor-memory lane per thread); 12 issues TMA;
 // 13 issues tcgen05.mma and owns the tensor-memory allocation.  Tensor memory
 // (512 columns): dV | dK | S^T (P^T) | dP^T (later dQ).  Shared memory: K, V,
-// two stages of Q and dO, the dS^T tile and the per-row L and D vectors.
+// two stages of Q (with its per-row L and D vectors), one of dO, the dS^T
+// tile and two 16 KB fp32 staging buffers for the dQ reduction.
+//
+// The dQ reduction is the costly exchange of this design: every key/value
+// tile adds a 128 x d fp32 partial into each query tile's accumulator.  Done
+// as one red.global per thread and 16 bytes it saturated the load/store path
+// that the softmax warps also use; as TMA tensor reduce-adds of 16 KB boxes it
+// is a handful of instructions per tile and runs on the copy engine.
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -42,18 +50,19 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kBarKV = 0;
 constexpr int kBarQFull = 1;     // + stage
 constexpr int kBarQEmpty = 3;    // + stage
-constexpr int kBarDOFull = 5;    // + stage
-constexpr int kBarDOEmpty = 7;   // + stage
-constexpr int kBarSFull = 9;
-constexpr int kBarPReady = 10;
-constexpr int kBarDPFull = 11;
-constexpr int kBarDSReady = 12;
-constexpr int kBarDSFree = 13;
-constexpr int kBarDQFull = 14;
-constexpr int kBarDQFree = 15;
-constexpr int kBarAccFull = 16;
-constexpr int kBarDrain = 17;
-constexpr int kNumBars = 18;
+constexpr int kBarDOFull = 5;
+constexpr int kBarDOEmpty = 6;
+constexpr int kBarSFull = 7;
+constexpr int kBarPReady = 8;
+constexpr int kBarDPFull = 9;
+constexpr int kBarDSReady = 10;
+constexpr int kBarDSFree = 11;
+constexpr int kBarDQFull = 12;
+constexpr int kBarDQFree = 13;
+constexpr int kBarAccFull = 14;
+constexpr int kBarDrain = 15;
+constexpr int kNumBars = 16;
+constexpr int kDrainBarrierId = 1;  // named barrier of the 128 dQ-drain threads
 
 template <int HD>
 struct Layout {
@@ -61,9 +70,10 @@ struct Layout {
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;          // + stage * kTileBytes
-  static constexpr int kDO = kQ + 2 * kTileBytes;     // + stage * kTileBytes
-  static constexpr int kDS = kDO + 2 * kTileBytes;    // 128 x 128 bf16, two 16 KB blocks
-  static constexpr int kVec = kDS + 32768;            // stage s: L2 at +1024 s, D at +1024 s + 512
+  static constexpr int kDO = kQ + 2 * kTileBytes;     // one stage
+  static constexpr int kDS = kDO + kTileBytes;        // 128 x 128 bf16, two 16 KB blocks
+  static constexpr int kStage = kDS + 32768;          // 2 x (128 rows x 32 fp32), swizzled
+  static constexpr int kVec = kStage + 32768;         // stage s: L2 at +1024 s, D at +1024 s + 512
   static constexpr int kBar = kVec + 2048;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -87,8 +97,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmdO, const float* __restrict__ L2ws,
-                         const float* __restrict__ Dws, float* __restrict__ acc,
+                         const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ CUtensorMap tmAcc, const float* __restrict__ L2ws,
+                         const float* __restrict__ Dws,
                          __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int BH,
                          int N, float scale, float scale_log2, int* err) {
   using Ly = Layout<HD>;
@@ -118,9 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarQFull + s), 1);
       mbar_init(bar(kBarQEmpty + s), 1);
-      mbar_init(bar(kBarDOFull + s), 1);
-      mbar_init(bar(kBarDOEmpty + s), 1);
     }
+    mbar_init(bar(kBarDOFull), 1);
+    mbar_init(bar(kBarDOEmpty), 1);
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarPReady), 256);
     mbar_init(bar(kBarDPFull), 1);
@@ -141,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmAcc);
   }
   tc_fence_before();
   __syncthreads();
@@ -151,6 +163,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop (warp-uniform operands); one lane issues.
+    // Order: K, V, Q(0); then per tile dO(it) (single buffer, free once
+    // dV(it-1) is done) and Q(it+1) (two stages, free once dK(it-1) is done).
+    auto load_q = [&](int i) {  // elected lane only
+      const int s = i & 1, qt = it0 + i;
+      mbar_arrive_expect_tx(bar(kBarQFull + s), Ly::kTileBytes + 1024);
+#pragma unroll
+      for (int cb = 0; cb < HD / 64; ++cb)
+        tma_load_3d(sbase + Ly::kQ + s * Ly::kTileBytes + cb * 16384, &tmQ, bar(kBarQFull + s),
+                    cb * 64, qt * 128, bh);
+      const size_t vo = size_t(bh) * Npad + size_t(qt) * 128;
+      bulk_load(sbase + Ly::kVec + s * 1024, L2ws + vo, 512, bar(kBarQFull + s));
+      bulk_load(sbase + Ly::kVec + s * 1024 + 512, Dws + vo, 512, bar(kBarQFull + s));
+    };
     if (elect_one()) {
       mbar_arrive_expect_tx(bar(kBarKV), 2 * Ly::kTileBytes);
 #pragma unroll
@@ -158,31 +183,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sbase + Ly::kK + cb * 16384, &tmK, bar(kBarKV), cb * 64, jt * 128, bh);
         tma_load_3d(sbase + Ly::kV + cb * 16384, &tmV, bar(kBarKV), cb * 64, jt * 128, bh);
       }
+      load_q(0);
     }
     __syncwarp();
     for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1, n = it >> 1, qt = it0 + it;
-      if (it >= 2 && !mbar_wait_warp(bar(kBarQEmpty + s), (n - 1) & 1, ctx, 0x210)) break;
+      if (it > 0 && !mbar_wait_warp(bar(kBarDOEmpty), (it - 1) & 1, ctx, 0x211)) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(bar(kBarQFull + s), Ly::kTileBytes + 1024);
+        mbar_arrive_expect_tx(bar(kBarDOFull), Ly::kTileBytes);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(sbase + Ly::kQ + s * Ly::kTileBytes + cb * 16384, &tmQ, bar(kBarQFull + s),
-                      cb * 64, qt * 128, bh);
-        const size_t vo = size_t(bh) * Npad + size_t(qt) * 128;
-        bulk_load(sbase + Ly::kVec + s * 1024, L2ws + vo, 512, bar(kBarQFull + s));
-        bulk_load(sbase + Ly::kVec + s * 1024 + 512, Dws + vo, 512, bar(kBarQFull + s));
+          tma_load_3d(sbase + Ly::kDO + cb * 16384, &tmdO, bar(kBarDOFull), cb * 64,
+                      (it0 + it) * 128, bh);
       }
       __syncwarp();
-      if (it >= 2 && !mbar_wait_warp(bar(kBarDOEmpty + s), (n - 1) & 1, ctx, 0x211)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(kBarDOFull + s), Ly::kTileBytes);
-#pragma unroll
-        for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(sbase + Ly::kDO + s * Ly::kTileBytes + cb * 16384, &tmdO,
-                      bar(kBarDOFull + s), cb * 64, qt * 128, bh);
+      const int nx = it + 1;
+      if (nx < n_it) {
+        if (nx >= 2 &&
+            !mbar_wait_warp(bar(kBarQEmpty + (nx & 1)), ((nx >> 1) - 1) & 1, ctx, 0x210))
+          break;
+        if (elect_one()) load_q(nx);
+        __syncwarp();
       }
-      __syncwarp();
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -202,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n_it && ok; ++it) {
       const int s = it & 1, ph = (it >> 1) & 1;
       const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
-      const uint32_t sDO = sbase + Ly::kDO + s * Ly::kTileBytes;
+      const uint32_t sDO = sbase + Ly::kDO;
       const uint64_t dQ_k = make_sdesc_sw128(sQ, 16, 1024), dQ_mn = make_sdesc_sw128(sQ, 16384, 1024);
       const uint64_t dO_k = make_sdesc_sw128(sDO, 16, 1024), dO_mn = make_sdesc_sw128(sDO, 16384, 1024);
       const uint32_t acc0 = it > 0 ? 1u : 0u;
@@ -219,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       // dP^T = V dO^T  (its columns held dQ of the previous tile: wait for the drain)
-      if (!(ok = mbar_wait_warp(bar(kBarDOFull + s), ph, ctx, 0x222))) break;
+      if (!(ok = mbar_wait_warp(bar(kBarDOFull), it & 1, ctx, 0x222))) break;
       if (it > 0 && !(ok = mbar_wait_warp(bar(kBarDQFree), (it - 1) & 1, ctx, 0x223))) break;
       tc_fence_after();
       if (elect_one()) {
@@ -240,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k)
           mma_ts(tDV, tS + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(dO_mn, k * 2048), kIdV,
                  k > 0 ? 1u : acc0);
-        tc_commit(bar(kBarDOEmpty + s));
+        tc_commit(bar(kBarDOEmpty));
       }
       __syncwarp();
       // dK += dS^T Q, then dQ_i = dS K into the dP^T columns
@@ -361,34 +382,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ drain
+    // Tensor memory -> registers -> swizzled fp32 staging tile -> TMA
+    // reduce-add into the accumulator, 32 columns (16 KB) per box, two
+    // staging buffers.  Thread 0 issues the reductions and owns their groups.
     const int r = threadIdx.x;  // query row within the tile = TMEM lane
     const uint32_t tDQ = tbase + (uint32_t(warp * 32) << 16) + Ly::kColDP;
+    const bool issuer = threadIdx.x == 0;
     for (int it = 0; it < n_it; ++it) {
       const int qt = it0 + it;
-      if (!mbar_wait_warp(bar(kBarDQFull), it & 1, ctx, 0x240)) break;
+      // The four drain warps agree before any named barrier below, so that a
+      // wait that gave up in one warp stops all of them.
+      const bool got = mbar_wait_warp(bar(kBarDQFull), it & 1, ctx, 0x240);
+      if (!named_barrier_and(kDrainBarrierId, 128, got)) break;
       tc_fence_after();
-      // accumulator layout [bh][tile][HD/8][128][8]
-      float* abase = acc + (size_t(bh) * n_tiles + qt) * (HD / 8) * 1024 + r * 8;
+      // Two 64-column halves (register budget): the columns are released to
+      // the MMA warp once the last half has been read.
 #pragma unroll
-      for (int half = 0; half < HD / 64; ++half) {
+      for (int h = 0; h < HD / 64; ++h) {
         uint32_t u[64];
-        tmem_ld32(tDQ + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tDQ + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        tmem_ld32(tDQ + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        tmem_ld32(tDQ + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
-        if (half == HD / 64 - 1) {
+        if (h == HD / 64 - 1) {
           tc_fence_before();
           mbar_arrive(bar(kBarDQFree));
         }
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          float* p = abase + (half * 8 + g) * 1024;
-          red_add_v4(p, __uint_as_float(u[8 * g]), __uint_as_float(u[8 * g + 1]),
-                     __uint_as_float(u[8 * g + 2]), __uint_as_float(u[8 * g + 3]));
-          red_add_v4(p + 4, __uint_as_float(u[8 * g + 4]), __uint_as_float(u[8 * g + 5]),
-                     __uint_as_float(u[8 * g + 6]), __uint_as_float(u[8 * g + 7]));
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * h + cc;
+          const uint32_t buf = sbase + Ly::kStage + (c & 1) * 16384;
+          // the reduction that last read this buffer (two boxes ago) is done reading
+          if (issuer) bulk_wait_group_read<1>();
+          named_barrier_sync(kDrainBarrierId, 128);
+          const uint32_t row = buf + r * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(row + ((j ^ (r & 7)) << 4), u[32 * cc + 4 * j], u[32 * cc + 4 * j + 1],
+                         u[32 * cc + 4 * j + 2], u[32 * cc + 4 * j + 3]);
+          fence_proxy_async_smem();
+          named_barrier_sync(kDrainBarrierId, 128);
+          if (issuer) {
+            tma_reduce_add_2d(&tmAcc, buf, 32 * c, bh * Npad + qt * 128);
+            bulk_commit_group();
+          }
         }
       }
     }
+    if (issuer) bulk_wait_group_all();  // reductions complete before the CTA retires
   }
 
   // ---------------------------------------------------------------- teardown
@@ -451,20 +491,19 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ step 3
+// The accumulator is [BH][Npad][HD] fp32 (row-major); each thread converts 8
+// consecutive values of one row.
 template <int HD>
 __global__ void __launch_bounds__(256)
     attn_bwd_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dQ,
-                               int BH, int N, int n_tiles, float scale) {
-  const size_t units = size_t(BH) * n_tiles * (HD / 8) * 128;
+                               int BH, int N, int Npad, float scale) {
+  const size_t units = size_t(BH) * Npad * (HD / 8);
   const size_t nthreads = size_t(gridDim.x) * blockDim.x;
   for (size_t u = size_t(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += nthreads) {
-    const int r = int(u & 127);
-    const size_t rest = u >> 7;
-    const int g = int(rest % (HD / 8));
-    const size_t bt = rest / (HD / 8);
-    const int qt = int(bt % n_tiles);
-    const int bh = int(bt / n_tiles);
-    const int q = qt * 128 + r;
+    const int g = int(u % (HD / 8));
+    const size_t row = u / (HD / 8);
+    const int q = int(row % Npad);
+    const int bh = int(row / Npad);
     if (q >= N) continue;
     const float4 a = *reinterpret_cast<const float4*>(acc + u * 8);
     const float4 b = *reinterpret_cast<const float4*>(acc + u * 8 + 4);
@@ -492,9 +531,10 @@ __global__ void attn_watchdog_kernel(int* err, uint64_t limit_ns) {
 
 template <int HD, bool CAUSAL>
 static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                                 const CUtensorMap& tmV, const CUtensorMap& tmdO, void* dK,
-                                 void* dV, const Workspace& ws, const Shape& s, float scale,
-                                 int* err, cudaStream_t stream) {
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                 const CUtensorMap& tmAcc, void* dK, void* dV,
+                                 const Workspace& ws, const Shape& s, float scale, int* err,
+                                 cudaStream_t stream) {
   using Ly = Layout<HD>;
   auto kern = attn_bwd_main_kernel<HD, CAUSAL>;
   cudaError_t e =
@@ -502,7 +542,7 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   if (e != cudaSuccess) return e;
   const dim3 grid(unsigned(s.n_tiles) * unsigned(s.BH));
   kern<<<grid, kThreads, Ly::kBytes, stream>>>(
-      tmQ, tmK, tmV, tmdO, ws.L2, ws.D, ws.acc, reinterpret_cast<__nv_bfloat16*>(dK),
+      tmQ, tmK, tmV, tmdO, tmAcc, ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, scale, scale * 1.4426950408889634f, err);
   return cudaGetLastError();
 }
@@ -534,31 +574,31 @@ cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                            const CUtensorMap& tmV, const CUtensorMap& tmdO, void* dK, void* dV,
-                            const Workspace& ws, const Shape& s, float scale, int* err,
-                            cudaStream_t stream) {
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                            const CUtensorMap& tmAcc, void* dK, void* dV, const Workspace& ws,
+                            const Shape& s, float scale, int* err, cudaStream_t stream) {
   if (s.d == 64)
-    return s.causal
-               ? bwd::launch_main_t<64, true>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err, stream)
-               : bwd::launch_main_t<64, false>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err,
-                                               stream);
-  return s.causal
-             ? bwd::launch_main_t<128, true>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err, stream)
-             : bwd::launch_main_t<128, false>(tmQ, tmK, tmV, tmdO, dK, dV, ws, s, scale, err,
-                                              stream);
+    return s.causal ? bwd::launch_main_t<64, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
+                                                   scale, err, stream)
+                    : bwd::launch_main_t<64, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
+                                                    scale, err, stream);
+  return s.causal ? bwd::launch_main_t<128, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
+                                                  scale, err, stream)
+                  : bwd::launch_main_t<128, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
+                                                   scale, err, stream);
 }
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,
                                   cudaStream_t stream) {
-  const size_t units = size_t(s.BH) * s.n_tiles * (s.d / 8) * 128;
+  const size_t units = size_t(s.BH) * s.Npad * (s.d / 8);
   const unsigned grid = bwd::grid_for(units, 256);
   auto q = reinterpret_cast<__nv_bfloat16*>(dQ);
   if (s.d == 64)
-    bwd::attn_bwd_dq_convert_kernel<64><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N,
-                                                                  s.n_tiles, scale);
+    bwd::attn_bwd_dq_convert_kernel<64><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N, s.Npad,
+                                                                  scale);
   else
-    bwd::attn_bwd_dq_convert_kernel<128><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N,
-                                                                   s.n_tiles, scale);
+    bwd::attn_bwd_dq_convert_kernel<128><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N, s.Npad,
+                                                                   scale);
   return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@ struct Shape {
 // Workspace carve-up (all fp32, 256-byte aligned sections):
 //   L2  [BH][Npad]            L * log2(e); +inf on padded rows
 //   D   [BH][Npad]            rowsum(dO o O); 0 on padded rows
-//   acc [BH][n_tiles][d/8][128][8]   dQ accumulator (unscaled)
+//   acc [BH][Npad][d]         dQ accumulator (unscaled), row-major
 struct Workspace {
   float* L2;
   float* D;
@@ -36,6 +36,10 @@ Workspace carve_workspace(void* base, const Shape& s);
 // 64 x 128 x 1 box and 128-byte swizzle.  Returns 0 on success.
 int make_tile_map(CUtensorMap* map, const void* ptr, const Shape& s);
 
+// Encodes a 2-D fp32 tensor map over the dQ accumulator [BH*Npad][d] with a
+// 32 x 128 box (128-byte rows) and 128-byte swizzle, for TMA reduce-add.
+int make_acc_map(CUtensorMap* map, const float* acc, const Shape& s);
+
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        void* O, float* L, const Shape& s, float scale, int* err,
                        cudaStream_t stream);
@@ -44,9 +48,9 @@ cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
                                   const Workspace& ws, const Shape& s, cudaStream_t stream);
 
 cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                            const CUtensorMap& tmV, const CUtensorMap& tmdO, void* dK, void* dV,
-                            const Workspace& ws, const Shape& s, float scale, int* err,
-                            cudaStream_t stream);
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                            const CUtensorMap& tmAcc, void* dK, void* dV, const Workspace& ws,
+                            const Shape& s, float scale, int* err, cudaStream_t stream);
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,
                                   cudaStream_t stream);
