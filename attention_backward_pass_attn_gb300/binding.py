@@ -25,6 +25,7 @@ ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_WORKSPACE = 5
 ATTN_ERR_DEVICE = 6
+ATTN_ERR_TOO_LARGE = 7
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +59,7 @@ def load_library(path: str | None = None):
             "attn_bwd_preprocess": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
             "attn_bwd_main": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_dq_convert": (i, [vp, i, i, i, i, f, vp, sz, vp]),
+            "attn_bwd_noalloc": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]),
             "attn_last_device_error": (i, [vp]),
             "attn_device_error_word": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
             "attn_watchdog_selftest": (i, [ctypes.c_uint64, vp]),

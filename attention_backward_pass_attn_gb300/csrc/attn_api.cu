@@ -155,6 +155,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_TIMEOUT: return "device wait timed out";
     case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case ATTN_ERR_DEVICE: return "device-side check failed";
+    case ATTN_ERR_TOO_LARGE: return "problem too large for the built-in 32 MiB scratch";
     default: return "unknown status";
   }
 }

@@ -54,7 +54,8 @@ typedef enum {
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
   ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out (reported by attn_last_device_error) */
   ATTN_ERR_WORKSPACE = 5,   /* workspace NULL, misaligned or smaller than attn_bwd_workspace_size */
-  ATTN_ERR_DEVICE = 6       /* another device-side check failed (see attn_device_error_word) */
+  ATTN_ERR_DEVICE = 6,      /* another device-side check failed (see attn_device_error_word) */
+  ATTN_ERR_TOO_LARGE = 7    /* attn_bwd_noalloc: workspace need exceeds its built-in scratch */
 } attn_status_t;
 
 /*
@@ -112,6 +113,26 @@ int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, v
  */
 int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
                         size_t workspace_bytes, void* stream);
+
+/*
+ * Backward without any device allocation, for callers that cannot call
+ * cudaMalloc (a host framework whose allocator owns all device memory and
+ * hands a plug-in only its tensors, or a latency-bound loop that cannot
+ * afford cudaMalloc's implicit synchronisation).  The paper has no
+ * counterpart: this is an interface variant of attn_bwd, not part of the
+ * method.  Same arguments, results and errors as attn_bwd, without the
+ * workspace: the library uses a 32 MiB scratch array of its own in device
+ * memory, held by every GPU that loads the library until the process exits.
+ * Problems whose attn_bwd_workspace_size exceeds 32 MiB return
+ * ATTN_ERR_TOO_LARGE and launch nothing.  The first call on each device looks
+ * up the scratch's device address; make it before any stream capture on that
+ * device.  All calls share the scratch (it keeps the last call's contents,
+ * and every call rewrites what it reads), so calls that overlap on the GPU,
+ * e.g. on two streams, race: order them on one stream.
+ */
+int attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                     int causal, float scale, void* stream);
 
 /*
  * Synchronise `stream`, then read and clear the current device's error word.
