@@ -219,26 +219,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dS_mn = make_sdesc_sw128(sbase + Ly::kDS, 16384, 1024);   // dS, MN-major
     const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
     const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
-    bool ok = mbar_wait_warp(bar(kBarKV), 0, ctx, 0x220);
+    // Issue order per query tile it:  dP(it), dV(it), S(it+1), dK(it), dQ(it).
+    // S(it+1) goes right after dV(it) (which has consumed P(it) from the S
+    // columns; the softmax warps keep P(it) in registers), so the softmax
+    // warps compute P(it+1) while the tensor core runs dK(it) and dQ(it).
+    auto issue_s = [&](int stage) {  // S^T = K Q^T; elected lane only
+      const uint64_t dq = make_sdesc_sw128(sbase + Ly::kQ + stage * Ly::kTileBytes, 16, 1024);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+        mma_ss(tS, sdesc_add(dK_k, off), sdesc_add(dq, off), kIdS, k > 0 ? 1u : 0u);
+      }
+      tc_commit(bar(kBarSFull));
+    };
+    bool ok = mbar_wait_warp(bar(kBarKV), 0, ctx, 0x220) &&
+              mbar_wait_warp(bar(kBarQFull), 0, ctx, 0x221);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) issue_s(0);
+      __syncwarp();
+    }
     for (int it = 0; it < n_it && ok; ++it) {
-      const int s = it & 1, ph = (it >> 1) & 1;
+      const int s = it & 1;
       const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
       const uint32_t sDO = sbase + Ly::kDO;
-      const uint64_t dQ_k = make_sdesc_sw128(sQ, 16, 1024), dQ_mn = make_sdesc_sw128(sQ, 16384, 1024);
+      const uint64_t dQ_mn = make_sdesc_sw128(sQ, 16384, 1024);
       const uint64_t dO_k = make_sdesc_sw128(sDO, 16, 1024), dO_mn = make_sdesc_sw128(sDO, 16384, 1024);
       const uint32_t acc0 = it > 0 ? 1u : 0u;
-      // S^T = K Q^T
-      if (!(ok = mbar_wait_warp(bar(kBarQFull + s), ph, ctx, 0x221))) break;
-      tc_fence_after();
-      if (elect_one()) {
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tS, sdesc_add(dK_k, off), sdesc_add(dQ_k, off), kIdS, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(kBarSFull));
-      }
-      __syncwarp();
       // dP^T = V dO^T  (its columns held dQ of the previous tile: wait for the drain)
       if (!(ok = mbar_wait_warp(bar(kBarDOFull), it & 1, ctx, 0x222))) break;
       if (it > 0 && !(ok = mbar_wait_warp(bar(kBarDQFree), (it - 1) & 1, ctx, 0x223))) break;
@@ -264,6 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(bar(kBarDOEmpty));
       }
       __syncwarp();
+      // S(it+1) into the S columns, behind dV(it) in the tensor core's order
+      if (it + 1 < n_it) {
+        const int s1 = (it + 1) & 1;
+        if (!(ok = mbar_wait_warp(bar(kBarQFull + s1), ((it + 1) >> 1) & 1, ctx, 0x226))) break;
+        tc_fence_after();
+        if (elect_one()) issue_s(s1);
+        __syncwarp();
+      }
       // dK += dS^T Q, then dQ_i = dS K into the dP^T columns
       if (!(ok = mbar_wait_warp(bar(kBarDSReady), it & 1, ctx, 0x225))) break;
       tc_fence_after();
@@ -306,22 +321,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float* L2v = reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024) + 64 * h;
       const float* Dv = reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024 + 512) + 64 * h;
+      // P(it) stays in registers (packed bf16) for the dS phase: the tensor
+      // core overwrites these S columns with S(it+1) once dV(it) has read it.
+      uint32_t pk[32];
       {
         uint32_t u[64];
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
         tmem_wait_ld();
         const bool diag = CAUSAL && qt == jt;
-        uint32_t pk[32];
+        const float4* L2v4 = reinterpret_cast<const float4*>(L2v);
 #pragma unroll
-        for (int c2 = 0; c2 < 32; ++c2) {
-          float p0 = ex2(fmaf(__uint_as_float(u[2 * c2]), scale_log2, -L2v[2 * c2]));
-          float p1 = ex2(fmaf(__uint_as_float(u[2 * c2 + 1]), scale_log2, -L2v[2 * c2 + 1]));
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l = L2v4[c4];  // one broadcast load for four query columns
+          float p0 = ex2(fmaf(__uint_as_float(u[4 * c4]), scale_log2, -l.x));
+          float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), scale_log2, -l.y));
+          float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), scale_log2, -l.z));
+          float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), scale_log2, -l.w));
           if (diag) {  // key row r is visible to query columns >= r only
-            if (64 * h + 2 * c2 < r) p0 = 0.f;
-            if (64 * h + 2 * c2 + 1 < r) p1 = 0.f;
+            const int q0 = 64 * h + 4 * c4;
+            if (q0 < r) p0 = 0.f;
+            if (q0 + 1 < r) p1 = 0.f;
+            if (q0 + 2 < r) p2 = 0.f;
+            if (q0 + 3 < r) p3 = 0.f;
           }
-          pk[c2] = pack_bf16x2(p0, p1);
+          pk[2 * c4] = pack_bf16x2(p0, p1);
+          pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
         }
         tmem_st32(tS, pk);
         tmem_wait_st();
@@ -332,24 +357,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it > 0 && !(ok = mbar_wait_warp(bar(kBarDSFree), (it - 1) & 1, ctx, 0x233))) break;
       tc_fence_after();
       {
-        uint32_t u[64], pk[32];
-        tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_ld32(tS, pk);
-        tmem_wait_ld();
-        uint32_t ds[32];
+        const float4* Dv4 = reinterpret_cast<const float4*>(Dv);
+        // two 32-column chunks of dP^T; row r of the dS^T tile, 128-byte
+        // swizzle: 16-byte chunk c of the row lands at c ^ (r % 8)
 #pragma unroll
-        for (int c2 = 0; c2 < 32; ++c2) {
-          const float p0 = bf16lo_to_f32(pk[c2]), p1 = bf16hi_to_f32(pk[c2]);
-          const float ds0 = p0 * (__uint_as_float(u[2 * c2]) - Dv[2 * c2]);
-          const float ds1 = p1 * (__uint_as_float(u[2 * c2 + 1]) - Dv[2 * c2 + 1]);
-          ds[c2] = pack_bf16x2(ds0, ds1);
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t u[32];
+          tmem_ld32(tDP + 32 * ch, u);
+          tmem_wait_ld();
+          uint32_t ds[16];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 dd = Dv4[8 * ch + c4];  // one broadcast load for four query columns
+            const uint32_t pa = pk[16 * ch + 2 * c4], pb = pk[16 * ch + 2 * c4 + 1];
+            ds[2 * c4] = pack_bf16x2(bf16lo_to_f32(pa) * (__uint_as_float(u[4 * c4]) - dd.x),
+                                     bf16hi_to_f32(pa) * (__uint_as_float(u[4 * c4 + 1]) - dd.y));
+            ds[2 * c4 + 1] =
+                pack_bf16x2(bf16lo_to_f32(pb) * (__uint_as_float(u[4 * c4 + 2]) - dd.z),
+                            bf16hi_to_f32(pb) * (__uint_as_float(u[4 * c4 + 3]) - dd.w));
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(sDSrow + (((4 * ch + c) ^ (r & 7)) << 4), ds[4 * c], ds[4 * c + 1],
+                         ds[4 * c + 2], ds[4 * c + 3]);
         }
-        // Row r of the dS^T tile, 128-byte swizzle: 16-byte chunk c lands at c ^ (r % 8).
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(sDSrow + ((c ^ (r & 7)) << 4), ds[4 * c], ds[4 * c + 1], ds[4 * c + 2],
-                       ds[4 * c + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(kBarDSReady));
@@ -395,37 +426,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = mbar_wait_warp(bar(kBarDQFull), it & 1, ctx, 0x240);
       if (!named_barrier_and(kDrainBarrierId, 128, got)) break;
       tc_fence_after();
-      // Two 64-column halves (register budget): the columns are released to
-      // the MMA warp once the last half has been read.
+      // 32-column chunks.  For d = 128, chunks 0-2 are loaded, chunk 0 staged,
+      // chunk 3 loaded into chunk 0's registers, and only then are the columns
+      // released to the MMA warp (the register budget does not hold all four).
+      auto stage = [&](int c, const uint32_t (&v)[32]) {
+        const uint32_t buf = sbase + Ly::kStage + (c & 1) * 16384;
+        // the reduction that last read this buffer (two boxes ago) is done reading
+        if (issuer) bulk_wait_group_read<1>();
+        named_barrier_sync(kDrainBarrierId, 128);
+        const uint32_t row = buf + r * 128;
 #pragma unroll
-      for (int h = 0; h < HD / 64; ++h) {
-        uint32_t u[64];
-        tmem_ld32(tDQ + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tDQ + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(row + ((j ^ (r & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                       v[4 * j + 3]);
+        fence_proxy_async_smem();
+        named_barrier_sync(kDrainBarrierId, 128);
+        if (issuer) {
+          tma_reduce_add_2d(&tmAcc, buf, 32 * c, bh * Npad + qt * 128);
+          bulk_commit_group();
+        }
+      };
+      uint32_t a0[32], a1[32];
+      tmem_ld32(tDQ, a0);
+      tmem_ld32(tDQ + 32, a1);
+      if constexpr (HD == 128) {
+        uint32_t a2[32];
+        tmem_ld32(tDQ + 64, a2);
         tmem_wait_ld();
-        if (h == HD / 64 - 1) {
-          tc_fence_before();
-          mbar_arrive(bar(kBarDQFree));
-        }
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * h + cc;
-          const uint32_t buf = sbase + Ly::kStage + (c & 1) * 16384;
-          // the reduction that last read this buffer (two boxes ago) is done reading
-          if (issuer) bulk_wait_group_read<1>();
-          named_barrier_sync(kDrainBarrierId, 128);
-          const uint32_t row = buf + r * 128;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(row + ((j ^ (r & 7)) << 4), u[32 * cc + 4 * j], u[32 * cc + 4 * j + 1],
-                         u[32 * cc + 4 * j + 2], u[32 * cc + 4 * j + 3]);
-          fence_proxy_async_smem();
-          named_barrier_sync(kDrainBarrierId, 128);
-          if (issuer) {
-            tma_reduce_add_2d(&tmAcc, buf, 32 * c, bh * Npad + qt * 128);
-            bulk_commit_group();
-          }
-        }
+        stage(0, a0);
+        tmem_ld32(tDQ + 96, a0);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kBarDQFree));
+        stage(1, a1);
+        stage(2, a2);
+        stage(3, a0);
+      } else {
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(kBarDQFree));
+        stage(0, a0);
+        stage(1, a1);
       }
     }
     if (issuer) bulk_wait_group_all();  // reductions complete before the CTA retires
