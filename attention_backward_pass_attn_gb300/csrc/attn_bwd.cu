@@ -219,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dS_mn = make_sdesc_sw128(sbase + Ly::kDS, 16384, 1024);   // dS, MN-major
     const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
     const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
-    // Issue order per query tile it:  dP(it), dV(it), S(it+1), dK(it), dQ(it).
+    // Issue order per query tile it:  dP(it), dV(it), S(it+1), then dK(it) and
+    // dQ(it) (order chosen by head dimension, below).
     // S(it+1) goes right after dV(it) (which has consumed P(it) from the S
     // columns; the softmax warps keep P(it) in registers), so the softmax
     // warps compute P(it+1) while the tensor core runs dK(it) and dQ(it).
@@ -279,20 +280,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) issue_s(s1);
         __syncwarp();
       }
-      // dK += dS^T Q, then dQ_i = dS K into the dP^T columns
+      // dK += dS^T Q and dQ_i = dS K (into the dP^T columns).  For d = 64, dQ
+      // goes first so that the drain warps empty those columns while dK runs
+      // and dP(it+1) finds them free (measured faster); for d = 128 the two
+      // orders measure within noise of each other and dK goes first.
+      constexpr bool kDqFirst = HD == 64;
       if (!(ok = mbar_wait_warp(bar(kBarDSReady), it & 1, ctx, 0x225))) break;
       tc_fence_after();
       if (elect_one()) {
+        auto issue_dq = [&] {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tDP, sdesc_add(dS_mn, k * 2048), sdesc_add(dK_mn, k * 2048), kIdQ,
+                   k > 0 ? 1u : 0u);
+          tc_commit(bar(kBarDQFull));
+        };
+        if (kDqFirst) issue_dq();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
           mma_ss(tDK, sdesc_add(dS_k, off), sdesc_add(dQ_mn, k * 2048), kIdV, k > 0 ? 1u : acc0);
         }
         tc_commit(bar(kBarQEmpty + s));
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tDP, sdesc_add(dS_mn, k * 2048), sdesc_add(dK_mn, k * 2048), kIdQ, k > 0 ? 1u : 0u);
-        tc_commit(bar(kBarDQFull));
+        if (!kDqFirst) issue_dq();
         tc_commit(bar(kBarDSFree));
       }
       __syncwarp();
@@ -365,16 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t u[32];
           tmem_ld32(tDP + 32 * ch, u);
           tmem_wait_ld();
+          // dS = P o (dP - D): the difference in fp32, packed once to bf16x2,
+          // times the packed bf16 P with one bf16x2 multiply per pair.
           uint32_t ds[16];
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 dd = Dv4[8 * ch + c4];  // one broadcast load for four query columns
-            const uint32_t pa = pk[16 * ch + 2 * c4], pb = pk[16 * ch + 2 * c4 + 1];
-            ds[2 * c4] = pack_bf16x2(bf16lo_to_f32(pa) * (__uint_as_float(u[4 * c4]) - dd.x),
-                                     bf16hi_to_f32(pa) * (__uint_as_float(u[4 * c4 + 1]) - dd.y));
-            ds[2 * c4 + 1] =
-                pack_bf16x2(bf16lo_to_f32(pb) * (__uint_as_float(u[4 * c4 + 2]) - dd.z),
-                            bf16hi_to_f32(pb) * (__uint_as_float(u[4 * c4 + 3]) - dd.w));
+            ds[2 * c4] = mul_bf16x2(pk[16 * ch + 2 * c4],
+                                    pack_bf16x2(__uint_as_float(u[4 * c4]) - dd.x,
+                                                __uint_as_float(u[4 * c4 + 1]) - dd.y));
+            ds[2 * c4 + 1] = mul_bf16x2(pk[16 * ch + 2 * c4 + 1],
+                                        pack_bf16x2(__uint_as_float(u[4 * c4 + 2]) - dd.z,
+                                                    __uint_as_float(u[4 * c4 + 3]) - dd.w));
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c)
