@@ -386,6 +386,7 @@ def run_ours(args):
         "fwd_tflops": round(w.fwd_flops() / statistics.mean(res["fwd"]) / 1e9, 2),
         "bwd_ms": round(bwd_ms_total / args.steps, 5),
         "fwd_ms": round(sum(res["fwd"]) / args.steps, 5),
+        "bwd_fwd_time_ratio": round(sum(res["bwd"]) / max(sum(res["fwd"]), 1e-9), 3),
         "wall_s_timed_region": round(wall_s, 3),
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
