@@ -25,7 +25,9 @@
 // Warp roles of the main kernel (14 warps): 0-3 drain dQ from tensor memory
 // into the accumulator; 4-7 and 8-11 each own 64 of the 128 query columns of
 // S^T/dP^T (one key row = one tensor-memory lane per thread); 12 issues TMA;
-// 13 issues tcgen05.mma and owns the tensor-memory allocation.  Tensor memory
+// 13 issues tcgen05.mma and owns the tensor-memory allocation.  The grid is
+// persistent: each CTA walks a list of (head, key/value tile) work items, and
+// all barrier phases continue from one item to the next.  Tensor memory
 // (512 columns): dV | dK | S^T (P^T) | dP^T (later dQ).  Shared memory: K, V,
 // two stages of Q (with its per-row L and D vectors), one of dO, the dS^T
 // tile and two 16 KB fp32 staging buffers for the dQ reduction.
@@ -47,22 +49,38 @@ constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr int kBarKV = 0;
-constexpr int kBarQFull = 1;     // + stage
-constexpr int kBarQEmpty = 3;    // + stage
-constexpr int kBarDOFull = 5;
-constexpr int kBarDOEmpty = 6;
-constexpr int kBarSFull = 7;
-constexpr int kBarPReady = 8;
-constexpr int kBarDPFull = 9;
-constexpr int kBarDSReady = 10;
-constexpr int kBarDSFree = 11;
-constexpr int kBarDQFull = 12;
-constexpr int kBarDQFree = 13;
-constexpr int kBarAccFull = 14;
-constexpr int kBarDrain = 15;
-constexpr int kNumBars = 16;
+// Item-level barriers (one phase per work item of the CTA).
+constexpr int kBarKFull = 0;
+constexpr int kBarVFull = 1;
+constexpr int kBarKEmpty = 2;
+constexpr int kBarVEmpty = 3;
+constexpr int kBarAccFull = 4;    // dK, dV complete in tensor memory
+constexpr int kBarAccEmpty = 5;   // dK, dV read out by the epilogue
+// Tile-level barriers (one phase per query tile the CTA processes).
+constexpr int kBarQFull = 6;      // + stage
+constexpr int kBarQEmpty = 8;     // + stage
+constexpr int kBarDOFull = 10;
+constexpr int kBarDOEmpty = 11;
+constexpr int kBarSFull = 12;
+constexpr int kBarPReady = 13;
+constexpr int kBarDPFull = 14;
+constexpr int kBarDSReady = 15;
+constexpr int kBarDSFree = 16;
+constexpr int kBarDQFull = 17;
+constexpr int kBarDQFree = 18;
+constexpr int kBarDrain = 19;
+constexpr int kNumBars = 20;
 constexpr int kDrainBarrierId = 1;  // named barrier of the 128 dQ-drain threads
+
+// Work items are (head, key/value tile) pairs with index i = jt * BH + bh.
+// Under the causal mask a smaller jt sees more query tiles, so index order is
+// heaviest first.  The grid is persistent (at most one CTA per SM); CTA b of G
+// takes items b, 2G-1-b, 2G+b, 4G-1-b, ... (a snake over rounds, which evens
+// out the heavy-first order).  Returns -1 past the last item.
+__device__ __forceinline__ int snake_item(int k, int b, int G, int n_items) {
+  const int idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
+  return idx < n_items ? idx : -1;
+}
 
 template <int HD>
 struct Layout {
@@ -114,10 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_tiles = (N + 127) >> 7;
   const int Npad = n_tiles * 128;
-  const int bh = blockIdx.x % BH;
-  const int jt = blockIdx.x / BH;          // key/value tile (small first: heaviest when causal)
-  const int it0 = CAUSAL ? jt : 0;         // first query tile that sees this key tile
-  const int n_it = n_tiles - it0;
+  const int n_items = BH * n_tiles;
+  const int G = gridDim.x, b = blockIdx.x;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
@@ -125,22 +141,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar(kBarKV), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kBarQFull + s), 1);
-      mbar_init(bar(kBarQEmpty + s), 1);
+    for (int i = 0; i < kNumBars; ++i) {
+      // arrivals per phase: the 256 softmax threads, the 128 drain threads,
+      // or one (a TMA transaction or a tcgen05.commit)
+      const uint32_t count =
+          (i == kBarPReady || i == kBarDSReady || i == kBarAccEmpty) ? 256
+          : (i == kBarDQFree)                                          ? 128
+                                                                       : 1;
+      mbar_init(bar(i), count);
     }
-    mbar_init(bar(kBarDOFull), 1);
-    mbar_init(bar(kBarDOEmpty), 1);
-    mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarPReady), 256);
-    mbar_init(bar(kBarDPFull), 1);
-    mbar_init(bar(kBarDSReady), 256);
-    mbar_init(bar(kBarDSFree), 1);
-    mbar_init(bar(kBarDQFull), 1);
-    mbar_init(bar(kBarDQFree), 128);
-    mbar_init(bar(kBarAccFull), 1);
-    mbar_init(bar(kBarDrain), 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -163,47 +172,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop (warp-uniform operands); one lane issues.
-    // Order: K, V, Q(0); then per tile dO(it) (single buffer, free once
-    // dV(it-1) is done) and Q(it+1) (two stages, free once dK(it-1) is done).
-    auto load_q = [&](int i) {  // elected lane only
-      const int s = i & 1, qt = it0 + i;
+    // Per item: V (free once the previous item's last dP is done), K (free
+    // once its last dK/dQ is done); per query tile g: dO(g) (single buffer,
+    // free once dV(g-1) is done) and Q(g+1) with its L and D vectors (two
+    // stages, free once dK(g-1) is done) -- for the last tile of an item,
+    // Q(g+1) is the first query tile of the next item.
+    auto load_q = [&](int g, int qbh, int qt) {  // elected lane only
+      const int s = g & 1;
       mbar_arrive_expect_tx(bar(kBarQFull + s), Ly::kTileBytes + 1024);
 #pragma unroll
       for (int cb = 0; cb < HD / 64; ++cb)
         tma_load_3d(sbase + Ly::kQ + s * Ly::kTileBytes + cb * 16384, &tmQ, bar(kBarQFull + s),
-                    cb * 64, qt * 128, bh);
-      const size_t vo = size_t(bh) * Npad + size_t(qt) * 128;
+                    cb * 64, qt * 128, qbh);
+      const size_t vo = size_t(qbh) * Npad + size_t(qt) * 128;
       bulk_load(sbase + Ly::kVec + s * 1024, L2ws + vo, 512, bar(kBarQFull + s));
       bulk_load(sbase + Ly::kVec + s * 1024 + 512, Dws + vo, 512, bar(kBarQFull + s));
     };
-    if (elect_one()) {
-      mbar_arrive_expect_tx(bar(kBarKV), 2 * Ly::kTileBytes);
-#pragma unroll
-      for (int cb = 0; cb < HD / 64; ++cb) {
-        tma_load_3d(sbase + Ly::kK + cb * 16384, &tmK, bar(kBarKV), cb * 64, jt * 128, bh);
-        tma_load_3d(sbase + Ly::kV + cb * 16384, &tmV, bar(kBarKV), cb * 64, jt * 128, bh);
-      }
-      load_q(0);
-    }
-    __syncwarp();
-    for (int it = 0; it < n_it; ++it) {
-      if (it > 0 && !mbar_wait_warp(bar(kBarDOEmpty), (it - 1) & 1, ctx, 0x211)) break;
+    bool ok = true;
+    int g = 0;
+    for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
+      const int jt = item / BH, bh = item % BH;
+      const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
+      const int next = snake_item(k + 1, b, G, n_items);
+      if (k > 0 && !(ok = mbar_wait_warp(bar(kBarVEmpty), (k - 1) & 1, ctx, 0x212))) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(bar(kBarDOFull), Ly::kTileBytes);
+        mbar_arrive_expect_tx(bar(kBarVFull), Ly::kTileBytes);
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
-          tma_load_3d(sbase + Ly::kDO + cb * 16384, &tmdO, bar(kBarDOFull), cb * 64,
-                      (it0 + it) * 128, bh);
+          tma_load_3d(sbase + Ly::kV + cb * 16384, &tmV, bar(kBarVFull), cb * 64, jt * 128, bh);
       }
       __syncwarp();
-      const int nx = it + 1;
-      if (nx < n_it) {
-        if (nx >= 2 &&
-            !mbar_wait_warp(bar(kBarQEmpty + (nx & 1)), ((nx >> 1) - 1) & 1, ctx, 0x210))
+      if (k > 0 && !(ok = mbar_wait_warp(bar(kBarKEmpty), (k - 1) & 1, ctx, 0x213))) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bar(kBarKFull), Ly::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < HD / 64; ++cb)
+          tma_load_3d(sbase + Ly::kK + cb * 16384, &tmK, bar(kBarKFull), cb * 64, jt * 128, bh);
+        if (k == 0) load_q(0, bh, it0);
+      }
+      __syncwarp();
+      for (int it = 0; it < n_it; ++it, ++g) {
+        if (g > 0 && !(ok = mbar_wait_warp(bar(kBarDOEmpty), (g - 1) & 1, ctx, 0x211))) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(kBarDOFull), Ly::kTileBytes);
+#pragma unroll
+          for (int cb = 0; cb < HD / 64; ++cb)
+            tma_load_3d(sbase + Ly::kDO + cb * 16384, &tmdO, bar(kBarDOFull), cb * 64,
+                        (it0 + it) * 128, bh);
+        }
+        __syncwarp();
+        int qbh = bh, qt = it0 + it + 1;
+        if (it + 1 == n_it) {
+          if (next < 0) continue;
+          qbh = next % BH;
+          qt = CAUSAL ? next / BH : 0;
+        }
+        const int gn = g + 1;
+        if (gn >= 2 &&
+            !(ok = mbar_wait_warp(bar(kBarQEmpty + (gn & 1)), ((gn >> 1) - 1) & 1, ctx, 0x210)))
           break;
-        if (elect_one()) load_q(nx);
+        if (elect_one()) load_q(gn, qbh, qt);
         __syncwarp();
       }
+      item = next;
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -219,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dS_mn = make_sdesc_sw128(sbase + Ly::kDS, 16384, 1024);   // dS, MN-major
     const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
     const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
-    // Issue order per query tile it:  dP(it), dV(it), S(it+1), then dK(it) and
-    // dQ(it) (order chosen by head dimension, below).
-    // S(it+1) goes right after dV(it) (which has consumed P(it) from the S
-    // columns; the softmax warps keep P(it) in registers), so the softmax
-    // warps compute P(it+1) while the tensor core runs dK(it) and dQ(it).
+    // Issue order per query tile:  dP, dV, S(next), then dK and dQ (order
+    // chosen by head dimension, below).  S(next) goes right behind dV (which
+    // has consumed P from the S columns; the softmax warps keep P in
+    // registers), so the softmax warps compute the next tile's P while the
+    // tensor core runs dK and dQ.  The first S of an item waits for its K.
     auto issue_s = [&](int stage) {  // S^T = K Q^T; elected lane only
       const uint64_t dq = make_sdesc_sw128(sbase + Ly::kQ + stage * Ly::kTileBytes, 16, 1024);
 #pragma unroll
@@ -233,84 +264,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(bar(kBarSFull));
     };
-    bool ok = mbar_wait_warp(bar(kBarKV), 0, ctx, 0x220) &&
-              mbar_wait_warp(bar(kBarQFull), 0, ctx, 0x221);
-    if (ok) {
+    // dK += dS^T Q and dQ_i = dS K (into the dP^T columns).  For d = 64, dQ
+    // goes first so that the drain warps empty those columns while dK runs
+    // and the next dP finds them free (measured faster); for d = 128 the two
+    // orders measure within noise of each other and dK goes first.
+    constexpr bool kDqFirst = HD == 64;
+    bool ok = true;
+    int g = 0;
+    for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
+      const int jt = item / BH;
+      const int n_it = n_tiles - (CAUSAL ? jt : 0);
+      if (!(ok = mbar_wait_warp(bar(kBarKFull), k & 1, ctx, 0x220))) break;
+      if (!(ok = mbar_wait_warp(bar(kBarQFull + (g & 1)), (g >> 1) & 1, ctx, 0x221))) break;
       tc_fence_after();
-      if (elect_one()) issue_s(0);
+      if (elect_one()) issue_s(g & 1);
       __syncwarp();
-    }
-    for (int it = 0; it < n_it && ok; ++it) {
-      const int s = it & 1;
-      const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
-      const uint32_t sDO = sbase + Ly::kDO;
-      const uint64_t dQ_mn = make_sdesc_sw128(sQ, 16384, 1024);
-      const uint64_t dO_k = make_sdesc_sw128(sDO, 16, 1024), dO_mn = make_sdesc_sw128(sDO, 16384, 1024);
-      const uint32_t acc0 = it > 0 ? 1u : 0u;
-      // dP^T = V dO^T  (its columns held dQ of the previous tile: wait for the drain)
-      if (!(ok = mbar_wait_warp(bar(kBarDOFull), it & 1, ctx, 0x222))) break;
-      if (it > 0 && !(ok = mbar_wait_warp(bar(kBarDQFree), (it - 1) & 1, ctx, 0x223))) break;
-      tc_fence_after();
-      if (elect_one()) {
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tDP, sdesc_add(dV_k, off), sdesc_add(dO_k, off), kIdS, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(kBarDPFull));
-      }
-      __syncwarp();
-      // dV += P^T dO, P^T read from tensor memory: query block k/4 was packed by
-      // the softmax warps of that half into its own first 32 columns.
-      if (!(ok = mbar_wait_warp(bar(kBarPReady), it & 1, ctx, 0x224))) break;
-      tc_fence_after();
-      if (elect_one()) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tDV, tS + 64 * (k >> 2) + 8 * (k & 3), sdesc_add(dO_mn, k * 2048), kIdV,
-                 k > 0 ? 1u : acc0);
-        tc_commit(bar(kBarDOEmpty));
-      }
-      __syncwarp();
-      // S(it+1) into the S columns, behind dV(it) in the tensor core's order
-      if (it + 1 < n_it) {
-        const int s1 = (it + 1) & 1;
-        if (!(ok = mbar_wait_warp(bar(kBarQFull + s1), ((it + 1) >> 1) & 1, ctx, 0x226))) break;
+      if (!(ok = mbar_wait_warp(bar(kBarVFull), k & 1, ctx, 0x227))) break;
+      for (int it = 0; it < n_it; ++it, ++g) {
+        const int s = g & 1;
+        const bool last = it + 1 == n_it;
+        const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
+        const uint32_t sDO = sbase + Ly::kDO;
+        const uint64_t dQ_mn = make_sdesc_sw128(sQ, 16384, 1024);
+        const uint64_t dO_k = make_sdesc_sw128(sDO, 16, 1024);
+        const uint64_t dO_mn = make_sdesc_sw128(sDO, 16384, 1024);
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
+        // dP^T = V dO^T  (its columns held the previous dQ: wait for the drain)
+        if (!(ok = mbar_wait_warp(bar(kBarDOFull), g & 1, ctx, 0x222))) break;
+        if (g > 0 && !(ok = mbar_wait_warp(bar(kBarDQFree), (g - 1) & 1, ctx, 0x223))) break;
         tc_fence_after();
-        if (elect_one()) issue_s(s1);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tDP, sdesc_add(dV_k, off), sdesc_add(dO_k, off), kIdS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(kBarDPFull));
+          if (last) tc_commit(bar(kBarVEmpty));
+        }
+        __syncwarp();
+        // dV += P^T dO, P^T read from tensor memory: query block kk/4 was
+        // packed by the softmax warps of that half into its own first 32
+        // columns.  The first dV of an item overwrites the accumulator: the
+        // previous item's epilogue must have read it.
+        if (!(ok = mbar_wait_warp(bar(kBarPReady), g & 1, ctx, 0x224))) break;
+        if (it == 0 && k > 0 &&
+            !(ok = mbar_wait_warp(bar(kBarAccEmpty), (k - 1) & 1, ctx, 0x228)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tDV, tS + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_add(dO_mn, kk * 2048), kIdV,
+                   kk > 0 ? 1u : acc0);
+          tc_commit(bar(kBarDOEmpty));
+        }
+        __syncwarp();
+        // S of the item's next query tile into the S columns, behind dV
+        if (!last) {
+          const int s1 = (g + 1) & 1;
+          if (!(ok = mbar_wait_warp(bar(kBarQFull + s1), ((g + 1) >> 1) & 1, ctx, 0x226)))
+            break;
+          tc_fence_after();
+          if (elect_one()) issue_s(s1);
+          __syncwarp();
+        }
+        if (!(ok = mbar_wait_warp(bar(kBarDSReady), g & 1, ctx, 0x225))) break;
+        tc_fence_after();
+        if (elect_one()) {
+          auto issue_dq = [&] {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tDP, sdesc_add(dS_mn, kk * 2048), sdesc_add(dK_mn, kk * 2048), kIdQ,
+                     kk > 0 ? 1u : 0u);
+            tc_commit(bar(kBarDQFull));
+          };
+          if (kDqFirst) issue_dq();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tDK, sdesc_add(dS_k, off), sdesc_add(dQ_mn, kk * 2048), kIdV,
+                   kk > 0 ? 1u : acc0);
+          }
+          tc_commit(bar(kBarQEmpty + s));
+          if (!kDqFirst) issue_dq();
+          tc_commit(bar(kBarDSFree));
+          if (last) {
+            tc_commit(bar(kBarKEmpty));
+            tc_commit(bar(kBarAccFull));
+          }
+        }
         __syncwarp();
       }
-      // dK += dS^T Q and dQ_i = dS K (into the dP^T columns).  For d = 64, dQ
-      // goes first so that the drain warps empty those columns while dK runs
-      // and dP(it+1) finds them free (measured faster); for d = 128 the two
-      // orders measure within noise of each other and dK goes first.
-      constexpr bool kDqFirst = HD == 64;
-      if (!(ok = mbar_wait_warp(bar(kBarDSReady), it & 1, ctx, 0x225))) break;
-      tc_fence_after();
-      if (elect_one()) {
-        auto issue_dq = [&] {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tDP, sdesc_add(dS_mn, k * 2048), sdesc_add(dK_mn, k * 2048), kIdQ,
-                   k > 0 ? 1u : 0u);
-          tc_commit(bar(kBarDQFull));
-        };
-        if (kDqFirst) issue_dq();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tDK, sdesc_add(dS_k, off), sdesc_add(dQ_mn, k * 2048), kIdV, k > 0 ? 1u : acc0);
-        }
-        tc_commit(bar(kBarQEmpty + s));
-        if (!kDqFirst) issue_dq();
-        tc_commit(bar(kBarDSFree));
-      }
-      __syncwarp();
+      item = snake_item(k + 1, b, G, n_items);
     }
-    if (elect_one()) {
-      tc_commit(bar(kBarAccFull));
-      tc_commit(bar(kBarDrain));
-    }
+    if (elect_one()) tc_commit(bar(kBarDrain));
     __syncwarp();
     volatile int never = 0;  // this wait ignores the CTA abort flag
     const WaitCtx own{&never, err, kWaitLimitNs};
@@ -324,82 +372,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tDP = tbase + lane_off + Ly::kColDP + 64 * h;
     const uint32_t sDSrow = sbase + Ly::kDS + h * 16384 + r * 128;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1, qt = it0 + it;
-      if (!(ok = mbar_wait_warp(bar(kBarQFull + s), (it >> 1) & 1, ctx, 0x230))) break;
-      if (!(ok = mbar_wait_warp(bar(kBarSFull), it & 1, ctx, 0x231))) break;
-      tc_fence_after();
-      const float* L2v = reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024) + 64 * h;
-      const float* Dv = reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024 + 512) + 64 * h;
-      // P(it) stays in registers (packed bf16) for the dS phase: the tensor
-      // core overwrites these S columns with S(it+1) once dV(it) has read it.
-      uint32_t pk[32];
-      {
-        uint32_t u[64];
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-        tmem_wait_ld();
-        const bool diag = CAUSAL && qt == jt;
-        const float4* L2v4 = reinterpret_cast<const float4*>(L2v);
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l = L2v4[c4];  // one broadcast load for four query columns
-          float p0 = ex2(fmaf(__uint_as_float(u[4 * c4]), scale_log2, -l.x));
-          float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), scale_log2, -l.y));
-          float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), scale_log2, -l.z));
-          float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), scale_log2, -l.w));
-          if (diag) {  // key row r is visible to query columns >= r only
-            const int q0 = 64 * h + 4 * c4;
-            if (q0 < r) p0 = 0.f;
-            if (q0 + 1 < r) p1 = 0.f;
-            if (q0 + 2 < r) p2 = 0.f;
-            if (q0 + 3 < r) p3 = 0.f;
-          }
-          pk[2 * c4] = pack_bf16x2(p0, p1);
-          pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
-        }
-        tmem_st32(tS, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(kBarPReady));
-      }
-      if (!(ok = mbar_wait_warp(bar(kBarDPFull), it & 1, ctx, 0x232))) break;
-      if (it > 0 && !(ok = mbar_wait_warp(bar(kBarDSFree), (it - 1) & 1, ctx, 0x233))) break;
-      tc_fence_after();
-      {
-        const float4* Dv4 = reinterpret_cast<const float4*>(Dv);
-        // two 32-column chunks of dP^T; row r of the dS^T tile, 128-byte
-        // swizzle: 16-byte chunk c of the row lands at c ^ (r % 8)
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t u[32];
-          tmem_ld32(tDP + 32 * ch, u);
+    int g = 0;
+    for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
+      const int jt = item / BH, bh = item % BH;
+      const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
+      for (int it = 0; it < n_it; ++it, ++g) {
+        const int s = g & 1, qt = it0 + it;
+        if (!(ok = mbar_wait_warp(bar(kBarQFull + s), (g >> 1) & 1, ctx, 0x230))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarSFull), g & 1, ctx, 0x231))) break;
+        tc_fence_after();
+        const float* L2v = reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024) + 64 * h;
+        const float* Dv =
+            reinterpret_cast<const float*>(smem + Ly::kVec + s * 1024 + 512) + 64 * h;
+        // P stays in registers (packed bf16) for the dS phase: the tensor
+        // core overwrites these S columns with the next S once dV has read it.
+        uint32_t pk[32];
+        {
+          uint32_t u[64];
+          tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+          tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
           tmem_wait_ld();
-          // dS = P o (dP - D): the difference in fp32, packed once to bf16x2,
-          // times the packed bf16 P with one bf16x2 multiply per pair.
-          uint32_t ds[16];
+          const bool diag = CAUSAL && qt == jt;
+          const float4* L2v4 = reinterpret_cast<const float4*>(L2v);
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 dd = Dv4[8 * ch + c4];  // one broadcast load for four query columns
-            ds[2 * c4] = mul_bf16x2(pk[16 * ch + 2 * c4],
-                                    pack_bf16x2(__uint_as_float(u[4 * c4]) - dd.x,
-                                                __uint_as_float(u[4 * c4 + 1]) - dd.y));
-            ds[2 * c4 + 1] = mul_bf16x2(pk[16 * ch + 2 * c4 + 1],
-                                        pack_bf16x2(__uint_as_float(u[4 * c4 + 2]) - dd.z,
-                                                    __uint_as_float(u[4 * c4 + 3]) - dd.w));
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l = L2v4[c4];  // one broadcast load for four query columns
+            float p0 = ex2(fmaf(__uint_as_float(u[4 * c4]), scale_log2, -l.x));
+            float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), scale_log2, -l.y));
+            float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), scale_log2, -l.z));
+            float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), scale_log2, -l.w));
+            if (diag) {  // key row r is visible to query columns >= r only
+              const int q0 = 64 * h + 4 * c4;
+              if (q0 < r) p0 = 0.f;
+              if (q0 + 1 < r) p1 = 0.f;
+              if (q0 + 2 < r) p2 = 0.f;
+              if (q0 + 3 < r) p3 = 0.f;
+            }
+            pk[2 * c4] = pack_bf16x2(p0, p1);
+            pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            st_shared_v4(sDSrow + (((4 * ch + c) ^ (r & 7)) << 4), ds[4 * c], ds[4 * c + 1],
-                         ds[4 * c + 2], ds[4 * c + 3]);
+          tmem_st32(tS, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(kBarPReady));
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(kBarDSReady));
+        if (!(ok = mbar_wait_warp(bar(kBarDPFull), g & 1, ctx, 0x232))) break;
+        if (g > 0 && !(ok = mbar_wait_warp(bar(kBarDSFree), (g - 1) & 1, ctx, 0x233))) break;
+        tc_fence_after();
+        {
+          const float4* Dv4 = reinterpret_cast<const float4*>(Dv);
+          // two 32-column chunks of dP^T; row r of the dS^T tile, 128-byte
+          // swizzle: 16-byte chunk c of the row lands at c ^ (r % 8)
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t u[32];
+            tmem_ld32(tDP + 32 * ch, u);
+            tmem_wait_ld();
+            // dS = P o (dP - D): the difference in fp32, packed once to
+            // bf16x2, times the packed bf16 P with one bf16x2 multiply per pair.
+            uint32_t ds[16];
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 dd = Dv4[8 * ch + c4];  // one broadcast load for four columns
+              ds[2 * c4] = mul_bf16x2(pk[16 * ch + 2 * c4],
+                                      pack_bf16x2(__uint_as_float(u[4 * c4]) - dd.x,
+                                                  __uint_as_float(u[4 * c4 + 1]) - dd.y));
+              ds[2 * c4 + 1] = mul_bf16x2(pk[16 * ch + 2 * c4 + 1],
+                                          pack_bf16x2(__uint_as_float(u[4 * c4 + 2]) - dd.z,
+                                                      __uint_as_float(u[4 * c4 + 3]) - dd.w));
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              st_shared_v4(sDSrow + (((4 * ch + c) ^ (r & 7)) << 4), ds[4 * c], ds[4 * c + 1],
+                           ds[4 * c + 2], ds[4 * c + 3]);
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(bar(kBarDSReady));
+        }
       }
-    }
-    // Epilogue: half 0 writes dV, half 1 writes dK (times the softmax scale).
-    if (ok && mbar_wait_warp(bar(kBarAccFull), 0, ctx, 0x238 + h)) {
+      if (!ok) break;
+      // Epilogue of the item: half 0 writes dV, half 1 writes dK (times the
+      // softmax scale), then the accumulators are released to the next item.
+      if (!(ok = mbar_wait_warp(bar(kBarAccFull), k & 1, ctx, 0x238 + h))) break;
       tc_fence_after();
       const int kv = jt * 128 + r;
       const uint32_t tAcc = tbase + lane_off + (h == 0 ? Ly::kColDV : Ly::kColDK);
@@ -422,6 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(bar(kBarAccEmpty));
+      item = snake_item(k + 1, b, G, n_items);
     }
   } else {
     // ------------------------------------------------------------ dQ drain
@@ -431,55 +489,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x;  // query row within the tile = TMEM lane
     const uint32_t tDQ = tbase + (uint32_t(warp * 32) << 16) + Ly::kColDP;
     const bool issuer = threadIdx.x == 0;
-    for (int it = 0; it < n_it; ++it) {
-      const int qt = it0 + it;
-      // The four drain warps agree before any named barrier below, so that a
-      // wait that gave up in one warp stops all of them.
-      const bool got = mbar_wait_warp(bar(kBarDQFull), it & 1, ctx, 0x240);
-      if (!named_barrier_and(kDrainBarrierId, 128, got)) break;
-      tc_fence_after();
-      // 32-column chunks.  For d = 128, chunks 0-2 are loaded, chunk 0 staged,
-      // chunk 3 loaded into chunk 0's registers, and only then are the columns
-      // released to the MMA warp (the register budget does not hold all four).
-      auto stage = [&](int c, const uint32_t (&v)[32]) {
-        const uint32_t buf = sbase + Ly::kStage + (c & 1) * 16384;
-        // the reduction that last read this buffer (two boxes ago) is done reading
-        if (issuer) bulk_wait_group_read<1>();
-        named_barrier_sync(kDrainBarrierId, 128);
-        const uint32_t row = buf + r * 128;
+    bool ok = true;
+    int g = 0;
+    for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
+      const int jt = item / BH, bh = item % BH;
+      const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
+      for (int it = 0; it < n_it; ++it, ++g) {
+        const int qt = it0 + it;
+        // The four drain warps agree before any named barrier below, so that a
+        // wait that gave up in one warp stops all of them.
+        const bool got = mbar_wait_warp(bar(kBarDQFull), g & 1, ctx, 0x240);
+        if (!(ok = named_barrier_and(kDrainBarrierId, 128, got))) break;
+        tc_fence_after();
+        // 32-column chunks.  For d = 128, chunks 0-2 are loaded, chunk 0
+        // staged, chunk 3 loaded into chunk 0's registers, and only then are
+        // the columns released to the MMA warp (the register budget does not
+        // hold all four).
+        auto stage = [&](int c, const uint32_t (&v)[32]) {
+          const uint32_t buf = sbase + Ly::kStage + (c & 1) * 16384;
+          // the reduction that last read this buffer (two boxes ago) is done
+          if (issuer) bulk_wait_group_read<1>();
+          named_barrier_sync(kDrainBarrierId, 128);
+          const uint32_t row = buf + r * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_shared_v4(row + ((j ^ (r & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                       v[4 * j + 3]);
-        fence_proxy_async_smem();
-        named_barrier_sync(kDrainBarrierId, 128);
-        if (issuer) {
-          tma_reduce_add_2d(&tmAcc, buf, 32 * c, bh * Npad + qt * 128);
-          bulk_commit_group();
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(row + ((j ^ (r & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                         v[4 * j + 3]);
+          fence_proxy_async_smem();
+          named_barrier_sync(kDrainBarrierId, 128);
+          if (issuer) {
+            tma_reduce_add_2d(&tmAcc, buf, 32 * c, bh * Npad + qt * 128);
+            bulk_commit_group();
+          }
+        };
+        uint32_t a0[32], a1[32];
+        tmem_ld32(tDQ, a0);
+        tmem_ld32(tDQ + 32, a1);
+        if constexpr (HD == 128) {
+          uint32_t a2[32];
+          tmem_ld32(tDQ + 64, a2);
+          tmem_wait_ld();
+          stage(0, a0);
+          tmem_ld32(tDQ + 96, a0);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(kBarDQFree));
+          stage(1, a1);
+          stage(2, a2);
+          stage(3, a0);
+        } else {
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(kBarDQFree));
+          stage(0, a0);
+          stage(1, a1);
         }
-      };
-      uint32_t a0[32], a1[32];
-      tmem_ld32(tDQ, a0);
-      tmem_ld32(tDQ + 32, a1);
-      if constexpr (HD == 128) {
-        uint32_t a2[32];
-        tmem_ld32(tDQ + 64, a2);
-        tmem_wait_ld();
-        stage(0, a0);
-        tmem_ld32(tDQ + 96, a0);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(kBarDQFree));
-        stage(1, a1);
-        stage(2, a2);
-        stage(3, a0);
-      } else {
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(kBarDQFree));
-        stage(0, a0);
-        stage(1, a1);
       }
+      item = snake_item(k + 1, b, G, n_items);
     }
     if (issuer) bulk_wait_group_all();  // reductions complete before the CTA retires
   }
@@ -582,6 +648,20 @@ __global__ void attn_watchdog_kernel(int* err, uint64_t limit_ns) {
   mbar_wait(smem_u32(&barrier), 0, ctx, 0xD06);
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+static int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int HD, bool CAUSAL>
 static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO,
@@ -593,7 +673,9 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid(unsigned(s.n_tiles) * unsigned(s.BH));
+  // Persistent grid: at most one CTA per SM, each walking its work items.
+  const long long n_items = (long long)s.n_tiles * s.BH;
+  const dim3 grid(unsigned(n_items < num_sms() ? n_items : num_sms()));
   kern<<<grid, kThreads, Ly::kBytes, stream>>>(
       tmQ, tmK, tmV, tmdO, tmAcc, ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, scale, scale * 1.4426950408889634f, err);
