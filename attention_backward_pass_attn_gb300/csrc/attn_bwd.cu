@@ -28,8 +28,10 @@
 // 13 issues tcgen05.mma and owns the tensor-memory allocation.  The grid is
 // persistent: each CTA walks a list of (head, key/value tile) work items, and
 // all barrier phases continue from one item to the next.  Tensor memory
-// (512 columns): dV | dK | S^T (P^T) | dP^T (later dQ).  Shared memory: K, V,
-// two stages of Q (with its per-row L and D vectors), one of dO, the dS^T
+// (512 columns): dV | dK | S^T (P^T) | dP^T | (dQ: its own columns for d = 64,
+// the dP^T columns for d = 128).  Shared memory: K, V,
+// two stages of Q (with its per-row L and D vectors), dO (two stages for
+// d = 64, one for d = 128), the dS^T
 // tile and two 16 KB fp32 staging buffers for the dQ reduction.
 //
 // The dQ reduction is the costly exchange of this design: every key/value
@@ -59,17 +61,17 @@ constexpr int kBarAccEmpty = 5;   // dK, dV read out by the epilogue
 // Tile-level barriers (one phase per query tile the CTA processes).
 constexpr int kBarQFull = 6;      // + stage
 constexpr int kBarQEmpty = 8;     // + stage
-constexpr int kBarDOFull = 10;
-constexpr int kBarDOEmpty = 11;
-constexpr int kBarSFull = 12;
-constexpr int kBarPReady = 13;
-constexpr int kBarDPFull = 14;
-constexpr int kBarDSReady = 15;
-constexpr int kBarDSFree = 16;
-constexpr int kBarDQFull = 17;
-constexpr int kBarDQFree = 18;
-constexpr int kBarDrain = 19;
-constexpr int kNumBars = 20;
+constexpr int kBarDOFull = 10;    // + dO stage
+constexpr int kBarDOEmpty = 12;   // + dO stage
+constexpr int kBarSFull = 14;
+constexpr int kBarPReady = 15;
+constexpr int kBarDPFull = 16;
+constexpr int kBarDSReady = 17;
+constexpr int kBarDSFree = 18;
+constexpr int kBarDQFull = 19;
+constexpr int kBarDQFree = 20;
+constexpr int kBarDrain = 21;
+constexpr int kNumBars = 22;
 constexpr int kDrainBarrierId = 1;  // named barrier of the 128 dQ-drain threads
 
 // Work items are (head, key/value tile) pairs with index i = jt * BH + bh.
@@ -88,8 +90,11 @@ struct Layout {
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;          // + stage * kTileBytes
-  static constexpr int kDO = kQ + 2 * kTileBytes;     // one stage
-  static constexpr int kDS = kDO + kTileBytes;        // 128 x 128 bf16, two 16 KB blocks
+  // dO: one stage for d = 128 (shared memory is full), two for d = 64, where
+  // the shorter tiles would otherwise wait for the next dO to arrive.
+  static constexpr int kDOStages = HD == 64 ? 2 : 1;
+  static constexpr int kDO = kQ + 2 * kTileBytes;     // + stage * kTileBytes
+  static constexpr int kDS = kDO + kDOStages * kTileBytes;  // 128 x 128 bf16, two 16 KB blocks
   static constexpr int kStage = kDS + 32768;          // 2 x (128 rows x 32 fp32), swizzled
   static constexpr int kVec = kStage + 32768;         // stage s: L2 at +1024 s, D at +1024 s + 512
   static constexpr int kBar = kVec + 2048;
@@ -103,6 +108,11 @@ struct Layout {
   static constexpr uint32_t kColDK = HD;
   static constexpr uint32_t kColS = 2 * HD;
   static constexpr uint32_t kColDP = 2 * HD + 128;
+  // d = 64 leaves 128 of the 512 columns free: dQ gets its own columns, so the
+  // next dP does not wait for the drain.  d = 128 has no room: dQ reuses the
+  // dP columns once the softmax warps have read them.
+  static constexpr bool kSeparateDq = HD == 64;
+  static constexpr uint32_t kColDQ = kSeparateDq ? 2 * HD + 256 : kColDP;
 };
 
 // Descriptor conventions (128-byte swizzle, tiles of 128 rows in 64-column
@@ -173,8 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop (warp-uniform operands); one lane issues.
     // Per item: V (free once the previous item's last dP is done), K (free
-    // once its last dK/dQ is done); per query tile g: dO(g) (single buffer,
-    // free once dV(g-1) is done) and Q(g+1) with its L and D vectors (two
+    // once its last dK/dQ is done); per query tile g: dO(g) (its stage is free
+    // once the dV of the tile that last held it is done) and Q(g+1) with its
+    // L and D vectors (two
     // stages, free once dK(g-1) is done) -- for the last tile of an item,
     // Q(g+1) is the first query tile of the next item.
     auto load_q = [&](int g, int qbh, int qt) {  // elected lane only
@@ -212,13 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       for (int it = 0; it < n_it; ++it, ++g) {
-        if (g > 0 && !(ok = mbar_wait_warp(bar(kBarDOEmpty), (g - 1) & 1, ctx, 0x211))) break;
+        const int ds_ = g % Ly::kDOStages, dn = g / Ly::kDOStages;
+        if (dn > 0 &&
+            !(ok = mbar_wait_warp(bar(kBarDOEmpty + ds_), (dn - 1) & 1, ctx, 0x211)))
+          break;
         if (elect_one()) {
-          mbar_arrive_expect_tx(bar(kBarDOFull), Ly::kTileBytes);
+          mbar_arrive_expect_tx(bar(kBarDOFull + ds_), Ly::kTileBytes);
 #pragma unroll
           for (int cb = 0; cb < HD / 64; ++cb)
-            tma_load_3d(sbase + Ly::kDO + cb * 16384, &tmdO, bar(kBarDOFull), cb * 64,
-                        (it0 + it) * 128, bh);
+            tma_load_3d(sbase + Ly::kDO + ds_ * Ly::kTileBytes + cb * 16384, &tmdO,
+                        bar(kBarDOFull + ds_), cb * 64, (it0 + it) * 128, bh);
         }
         __syncwarp();
         int qbh = bh, qt = it0 + it + 1;
@@ -250,11 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dS_mn = make_sdesc_sw128(sbase + Ly::kDS, 16384, 1024);   // dS, MN-major
     const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
     const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
-    // Issue order per query tile:  dP, dV, S(next), then dK and dQ (order
-    // chosen by head dimension, below).  S(next) goes right behind dV (which
-    // has consumed P from the S columns; the softmax warps keep P in
-    // registers), so the softmax warps compute the next tile's P while the
-    // tensor core runs dK and dQ.  The first S of an item waits for its K.
+    const uint32_t tDQ = tbase + Ly::kColDQ;
+    // Issue order per query tile:  dP, dV, S(next), dK, dQ.  S(next) goes right
+    // behind dV (which has consumed P from the S columns; the softmax warps
+    // keep P in registers), so the softmax warps compute the next tile's P
+    // while the tensor core runs dK and dQ.  The first S of an item waits for
+    // its K.
     auto issue_s = [&](int stage) {  // S^T = K Q^T; elected lane only
       const uint64_t dq = make_sdesc_sw128(sbase + Ly::kQ + stage * Ly::kTileBytes, 16, 1024);
 #pragma unroll
@@ -264,11 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(bar(kBarSFull));
     };
-    // dK += dS^T Q and dQ_i = dS K (into the dP^T columns).  For d = 64, dQ
-    // goes first so that the drain warps empty those columns while dK runs
-    // and the next dP finds them free (measured faster); for d = 128 the two
-    // orders measure within noise of each other and dK goes first.
-    constexpr bool kDqFirst = HD == 64;
+    // dK += dS^T Q, then dQ_i = dS K (into its own columns for d = 64, into
+    // the dP^T columns -- read by now -- for d = 128).
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
@@ -284,14 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = g & 1;
         const bool last = it + 1 == n_it;
         const uint32_t sQ = sbase + Ly::kQ + s * Ly::kTileBytes;
-        const uint32_t sDO = sbase + Ly::kDO;
+        const int ds_ = g % Ly::kDOStages;
+        const uint32_t sDO = sbase + Ly::kDO + ds_ * Ly::kTileBytes;
         const uint64_t dQ_mn = make_sdesc_sw128(sQ, 16384, 1024);
         const uint64_t dO_k = make_sdesc_sw128(sDO, 16, 1024);
         const uint64_t dO_mn = make_sdesc_sw128(sDO, 16384, 1024);
         const uint32_t acc0 = it > 0 ? 1u : 0u;
-        // dP^T = V dO^T  (its columns held the previous dQ: wait for the drain)
-        if (!(ok = mbar_wait_warp(bar(kBarDOFull), g & 1, ctx, 0x222))) break;
-        if (g > 0 && !(ok = mbar_wait_warp(bar(kBarDQFree), (g - 1) & 1, ctx, 0x223))) break;
+        // dP^T = V dO^T.  When dQ shares the dP columns, they held the previous
+        // dQ: wait for its drain.  (Otherwise the previous dP has been read:
+        // the softmax warps signalled DS_READY, which the last tile waited on.)
+        if (!(ok = mbar_wait_warp(bar(kBarDOFull + ds_), (g / Ly::kDOStages) & 1, ctx, 0x222)))
+          break;
+        if (!Ly::kSeparateDq && g > 0 &&
+            !(ok = mbar_wait_warp(bar(kBarDQFree), (g - 1) & 1, ctx, 0x223)))
+          break;
         tc_fence_after();
         if (elect_one()) {
 #pragma unroll
@@ -317,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tDV, tS + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_add(dO_mn, kk * 2048), kIdV,
                    kk > 0 ? 1u : acc0);
-          tc_commit(bar(kBarDOEmpty));
+          tc_commit(bar(kBarDOEmpty + ds_));
         }
         __syncwarp();
         // S of the item's next query tile into the S columns, behind dV
@@ -332,14 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(bar(kBarDSReady), g & 1, ctx, 0x225))) break;
         tc_fence_after();
         if (elect_one()) {
-          auto issue_dq = [&] {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tDP, sdesc_add(dS_mn, kk * 2048), sdesc_add(dK_mn, kk * 2048), kIdQ,
-                     kk > 0 ? 1u : 0u);
-            tc_commit(bar(kBarDQFull));
-          };
-          if (kDqFirst) issue_dq();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -347,7 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kk > 0 ? 1u : acc0);
           }
           tc_commit(bar(kBarQEmpty + s));
-          if (!kDqFirst) issue_dq();
+        }
+        __syncwarp();
+        // With its own columns, dQ waits only for the previous dQ's drain.
+        if (Ly::kSeparateDq && g > 0 &&
+            !(ok = mbar_wait_warp(bar(kBarDQFree), (g - 1) & 1, ctx, 0x223)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tDQ, sdesc_add(dS_mn, kk * 2048), sdesc_add(dK_mn, kk * 2048), kIdQ,
+                   kk > 0 ? 1u : 0u);
+          tc_commit(bar(kBarDQFull));
           tc_commit(bar(kBarDSFree));
           if (last) {
             tc_commit(bar(kBarKEmpty));
@@ -487,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // reduce-add into the accumulator, 32 columns (16 KB) per box, two
     // staging buffers.  Thread 0 issues the reductions and owns their groups.
     const int r = threadIdx.x;  // query row within the tile = TMEM lane
-    const uint32_t tDQ = tbase + (uint32_t(warp * 32) << 16) + Ly::kColDP;
+    const uint32_t tDQ = tbase + (uint32_t(warp * 32) << 16) + Ly::kColDQ;
     const bool issuer = threadIdx.x == 0;
     bool ok = true;
     int g = 0;
@@ -566,7 +588,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ step 1
 // One row per HD/8 threads (16 bytes each); rows beyond N get D = 0 and
-// L2 = +inf so that their recomputed probabilities are exactly 0.
+// L2 = +inf so that their recomputed probabilities are exactly 0.  Each
+// thread issues the loads of kUnroll rows before using any of them (memory
+// parallelism), then the accumulator is zeroed with 16-byte stores.
+constexpr int kUnroll = 4;
+
 template <int HD>
 __global__ void __launch_bounds__(256)
     attn_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ O,
@@ -576,33 +602,45 @@ __global__ void __launch_bounds__(256)
                                size_t acc_vec4) {
   constexpr int TPR = HD / 8;  // threads per row
   const size_t rows = size_t(BH) * Npad;
+  const size_t units = rows * TPR;
   const size_t nthreads = size_t(gridDim.x) * blockDim.x;
   const size_t gt = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  // rows: grid-stride in whole warps so the shuffle groups stay aligned
-  for (size_t base = (gt / 32) * 32; base < rows * TPR; base += nthreads) {
-    const size_t id = base + (gt & 31);
-    const size_t row = id / TPR;
-    const int sub = int(id % TPR);
-    float dot = 0.f;
-    const bool in = row < rows;
-    const int bh = in ? int(row / Npad) : 0;
-    const int q = in ? int(row % Npad) : 0;
-    const bool valid = in && q < N;
-    if (valid) {
-      const size_t off = (size_t(bh) * N + q) * HD + sub * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(O + off);
-      const uint4 b = *reinterpret_cast<const uint4*>(dO + off);
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+  const int lane = threadIdx.x & 31;
+  // Warp w covers units [w*32*kUnroll, (w+1)*32*kUnroll) per pass, so the
+  // shuffle groups of TPR lanes stay inside one row.
+  for (size_t base = (gt / 32) * 32 * kUnroll; base < units; base += nthreads * kUnroll) {
+    uint4 a[kUnroll], c[kUnroll];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        dot += bf16lo_to_f32(av[e]) * bf16lo_to_f32(bv[e]) +
-               bf16hi_to_f32(av[e]) * bf16hi_to_f32(bv[e]);
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t id = base + size_t(u) * 32 + lane;
+      const size_t row = id / TPR;
+      const int q = int(row % Npad);
+      a[u] = c[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (row < rows && q < N) {
+        const size_t off = (size_t(row / Npad) * N + q) * HD + int(id % TPR) * 8;
+        a[u] = __ldg(reinterpret_cast<const uint4*>(O + off));
+        c[u] = __ldg(reinterpret_cast<const uint4*>(dO + off));
+      }
     }
 #pragma unroll
-    for (int o = TPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if (in && sub == 0) {
-      Dws[row] = valid ? dot : 0.f;
-      L2ws[row] = valid ? L[size_t(bh) * N + q] * 1.4426950408889634f : INFINITY;
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t id = base + size_t(u) * 32 + lane;
+      const size_t row = id / TPR;
+      const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+      const uint32_t cv[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dot += bf16lo_to_f32(av[e]) * bf16lo_to_f32(cv[e]) +
+               bf16hi_to_f32(av[e]) * bf16hi_to_f32(cv[e]);
+#pragma unroll
+      for (int o = TPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (row < rows && id % TPR == 0) {
+        const int bh = int(row / Npad), q = int(row % Npad);
+        const bool valid = q < N;
+        Dws[row] = valid ? dot : 0.f;
+        L2ws[row] = valid ? __ldg(L + size_t(bh) * N + q) * 1.4426950408889634f : INFINITY;
+      }
     }
   }
   float4* a4 = reinterpret_cast<float4*>(acc);
@@ -610,25 +648,38 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ step 3
-// The accumulator is [BH][Npad][HD] fp32 (row-major); each thread converts 8
-// consecutive values of one row.
+// The accumulator is [BH][Npad][HD] fp32 (row-major); a unit is 8 consecutive
+// values of one row.  Each thread loads kUnroll units before storing any.
 template <int HD>
 __global__ void __launch_bounds__(256)
     attn_bwd_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dQ,
                                int BH, int N, int Npad, float scale) {
   const size_t units = size_t(BH) * Npad * (HD / 8);
   const size_t nthreads = size_t(gridDim.x) * blockDim.x;
-  for (size_t u = size_t(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += nthreads) {
-    const int g = int(u % (HD / 8));
-    const size_t row = u / (HD / 8);
-    const int q = int(row % Npad);
-    const int bh = int(row / Npad);
-    if (q >= N) continue;
-    const float4 a = *reinterpret_cast<const float4*>(acc + u * 8);
-    const float4 b = *reinterpret_cast<const float4*>(acc + u * 8 + 4);
-    st_global_v4(dQ + (size_t(bh) * N + q) * HD + g * 8, pack_bf16x2(a.x * scale, a.y * scale),
-                 pack_bf16x2(a.z * scale, a.w * scale), pack_bf16x2(b.x * scale, b.y * scale),
-                 pack_bf16x2(b.z * scale, b.w * scale));
+  for (size_t base = size_t(blockIdx.x) * blockDim.x + threadIdx.x; base < units;
+       base += nthreads * kUnroll) {
+    float4 a[kUnroll], c[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t id = base + size_t(u) * nthreads;
+      if (id < units) {
+        a[u] = __ldcs(reinterpret_cast<const float4*>(acc + id * 8));
+        c[u] = __ldcs(reinterpret_cast<const float4*>(acc + id * 8 + 4));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t id = base + size_t(u) * nthreads;
+      if (id >= units) continue;
+      const size_t row = id / (HD / 8);
+      const int q = int(row % Npad), bh = int(row / Npad);
+      if (q >= N) continue;
+      st_global_v4(dQ + (size_t(bh) * N + q) * HD + int(id % (HD / 8)) * 8,
+                   pack_bf16x2(a[u].x * scale, a[u].y * scale),
+                   pack_bf16x2(a[u].z * scale, a[u].w * scale),
+                   pack_bf16x2(c[u].x * scale, c[u].y * scale),
+                   pack_bf16x2(c[u].z * scale, c[u].w * scale));
+    }
   }
 }
 
