@@ -220,6 +220,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kK + cb * 16384, &tmK, bar(kBarKFull), cb * 64, jt * 128, bh);
         if (k == 0) load_q(0, bh, it0);
+        // Warm L2 (and the address translation) for the next item: a new head
+        // is often a cold region, and its first tiles are needed right at the
+        // item switch.
+        if (next >= 0) {
+          const int njt = next / BH, nbh = next % BH, nq = CAUSAL ? njt : 0;
+#pragma unroll
+          for (int cb = 0; cb < HD / 64; ++cb) {
+            tma_prefetch_3d(&tmK, cb * 64, njt * 128, nbh);
+            tma_prefetch_3d(&tmV, cb * 64, njt * 128, nbh);
+            tma_prefetch_3d(&tmQ, cb * 64, nq * 128, nbh);
+            tma_prefetch_3d(&tmdO, cb * 64, nq * 128, nbh);
+          }
+          const size_t vo = size_t(nbh) * Npad + size_t(nq) * 128;
+          bulk_prefetch(L2ws + vo, 512);
+          bulk_prefetch(Dws + vo, 512);
+        }
       }
       __syncwarp();
       for (int it = 0; it < n_it; ++it, ++g) {
