@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const WaitCtx ctx{abort_flag, err, kWaitLimitNs};
+  // Everything above overlaps the previous kernel; its results are read below.
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -622,6 +625,8 @@ __global__ void __launch_bounds__(256)
   const size_t nthreads = size_t(gridDim.x) * blockDim.x;
   const size_t gt = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
+  grid_dep_wait();  // O and L come from the forward
+  grid_dep_launch();
   // Warp w covers units [w*32*kUnroll, (w+1)*32*kUnroll) per pass, so the
   // shuffle groups of TPR lanes stay inside one row.
   for (size_t base = (gt / 32) * 32 * kUnroll; base < units; base += nthreads * kUnroll) {
@@ -672,6 +677,8 @@ __global__ void __launch_bounds__(256)
                                int BH, int N, int Npad, float scale) {
   const size_t units = size_t(BH) * Npad * (HD / 8);
   const size_t nthreads = size_t(gridDim.x) * blockDim.x;
+  grid_dep_wait();  // the accumulator is complete once the main kernel is
+  grid_dep_launch();
   for (size_t base = size_t(blockIdx.x) * blockDim.x + threadIdx.x; base < units;
        base += nthreads * kUnroll) {
     float4 a[kUnroll], c[kUnroll];
@@ -743,10 +750,10 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   // Persistent grid: at most one CTA per SM, each walking its work items.
   const long long n_items = (long long)s.n_tiles * s.BH;
   const dim3 grid(unsigned(n_items < num_sms() ? n_items : num_sms()));
-  kern<<<grid, kThreads, Ly::kBytes, stream>>>(
-      tmQ, tmK, tmV, tmdO, tmAcc, ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
-      reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, scale, scale * 1.4426950408889634f, err);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV, tmdO, tmAcc,
+                       ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
+                       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, scale,
+                       scale * 1.4426950408889634f, err);
 }
 
 static unsigned grid_for(size_t work_items, int per_block) {
@@ -766,13 +773,9 @@ cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
   const unsigned grid = bwd::grid_for(work, 256);
   auto o = reinterpret_cast<const __nv_bfloat16*>(O);
   auto g = reinterpret_cast<const __nv_bfloat16*>(dO);
-  if (s.d == 64)
-    bwd::attn_bwd_preprocess_kernel<64>
-        <<<grid, 256, 0, stream>>>(o, g, L, ws.L2, ws.D, ws.acc, s.BH, s.N, s.Npad, acc_vec4);
-  else
-    bwd::attn_bwd_preprocess_kernel<128>
-        <<<grid, 256, 0, stream>>>(o, g, L, ws.L2, ws.D, ws.acc, s.BH, s.N, s.Npad, acc_vec4);
-  return cudaGetLastError();
+  auto kern = s.d == 64 ? bwd::attn_bwd_preprocess_kernel<64> : bwd::attn_bwd_preprocess_kernel<128>;
+  return launch_kernel(kern, dim3(grid), dim3(256), 0, stream, o, g, L, ws.L2, ws.D, ws.acc, s.BH,
+                       s.N, s.Npad, acc_vec4);
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
@@ -795,13 +798,9 @@ cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s,
   const size_t units = size_t(s.BH) * s.Npad * (s.d / 8);
   const unsigned grid = bwd::grid_for(units, 256);
   auto q = reinterpret_cast<__nv_bfloat16*>(dQ);
-  if (s.d == 64)
-    bwd::attn_bwd_dq_convert_kernel<64><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N, s.Npad,
-                                                                  scale);
-  else
-    bwd::attn_bwd_dq_convert_kernel<128><<<grid, 256, 0, stream>>>(ws.acc, q, s.BH, s.N, s.Npad,
-                                                                   scale);
-  return cudaGetLastError();
+  auto kern = s.d == 64 ? bwd::attn_bwd_dq_convert_kernel<64> : bwd::attn_bwd_dq_convert_kernel<128>;
+  return launch_kernel(kern, dim3(grid), dim3(256), 0, stream, static_cast<const float*>(ws.acc), q,
+                       s.BH, s.N, s.Npad, scale);
 }
 
 cudaError_t launch_watchdog_selftest(int* err, uint64_t limit_ns, cudaStream_t stream) {

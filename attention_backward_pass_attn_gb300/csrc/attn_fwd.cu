@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const WaitCtx ctx{abort_flag, err, kWaitLimitNs};
+  // Everything above overlaps the previous kernel; its results are read below.
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -369,10 +372,8 @@ static cudaError_t launch_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   const int n_pairs = (s.n_tiles + 1) / 2;
   const dim3 grid(unsigned(n_pairs) * unsigned(s.BH));
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, Ly::kBytes, stream>>>(tmQ, tmK, tmV,
-                                               reinterpret_cast<__nv_bfloat16*>(O), L, s.BH, s.N,
-                                               scale_log2, err);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV,
+                       reinterpret_cast<__nv_bfloat16*>(O), L, s.BH, s.N, scale_log2, err);
 }
 
 }  // namespace fwd

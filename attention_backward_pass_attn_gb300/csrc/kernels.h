@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace attn {
 
 // One attention problem: BH = B*H independent heads of N rows, head dim d.
@@ -28,6 +30,28 @@ struct Workspace {
   float* D;
   float* acc;
 };
+
+// Launches a kernel of this library with programmatic dependent launch
+// allowed: the kernel may start while the previous kernel in the stream is
+// finishing.  Every kernel of the library executes griddepcontrol.wait before
+// it reads global memory that earlier work wrote, so results are the same as
+// with plain stream order; what overlaps is the launch latency and the
+// prologue (barrier set-up, tensor-memory allocation).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 size_t workspace_bytes(const Shape& s);
 Workspace carve_workspace(void* base, const Shape& s);

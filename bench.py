@@ -183,8 +183,14 @@ def barrier():
 
 
 # ----------------------------------------------------------------------------- our arm
-def time_workload(w, steps: int, warmup: int, flush, with_events=True):
-    """Run fwd + bwd `warmup + steps` times; returns per-step event times (ms)."""
+def time_workload(w, steps: int, warmup: int, flush, split=False):
+    """Run fwd + bwd `warmup + steps` times; returns per-step event times (ms).
+
+    Events go before the forward, between forward and backward, and after the
+    backward.  With `split`, events also separate the three backward kernels,
+    giving each kernel's time -- but an event between two kernels stops the
+    next one from starting early (programmatic dependent launch), so the
+    backward is timed as a whole without them."""
     import torch
 
     from attention_backward_pass_attn_gb300 import binding as ab
@@ -201,11 +207,15 @@ def time_workload(w, steps: int, warmup: int, flush, with_events=True):
     def step():
         ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream)
         e[1].record(stream)
-        ab.attn_bwd_preprocess(o, do, lse, ws, stream=stream)
-        e[2].record(stream)
-        ab.attn_bwd_main(q, k, v, do, dk, dv, w.causal, ws, scale=w.scale, stream=stream)
-        e[3].record(stream)
-        ab.attn_bwd_dq_convert(dq, ws, scale=w.scale, stream=stream)
+        if split:
+            ab.attn_bwd_preprocess(o, do, lse, ws, stream=stream)
+            e[2].record(stream)
+            ab.attn_bwd_main(q, k, v, do, dk, dv, w.causal, ws, scale=w.scale, stream=stream)
+            e[3].record(stream)
+            ab.attn_bwd_dq_convert(dq, ws, scale=w.scale, stream=stream)
+        else:  # the public call: the same three kernels
+            ab.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
+                        workspace=ws, stream=stream)
 
     rec = []
     for i in range(warmup + steps):
@@ -222,13 +232,13 @@ def time_workload(w, steps: int, warmup: int, flush, with_events=True):
         raise RuntimeError("device error status %d during the benchmark" % st)
     out = {"fwd": [], "prep": [], "main": [], "conv": [], "bwd": [], "step": []}
     for e in rec:
-        t = [e[i].elapsed_time(e[i + 1]) for i in range(4)]
-        out["fwd"].append(t[0])
-        out["prep"].append(t[1])
-        out["main"].append(t[2])
-        out["conv"].append(t[3])
-        out["bwd"].append(t[1] + t[2] + t[3])
-        out["step"].append(sum(t))
+        out["fwd"].append(e[0].elapsed_time(e[1]))
+        out["bwd"].append(e[1].elapsed_time(e[4]))
+        out["step"].append(e[0].elapsed_time(e[4]))
+        if split:
+            out["prep"].append(e[1].elapsed_time(e[2]))
+            out["main"].append(e[2].elapsed_time(e[3]))
+            out["conv"].append(e[3].elapsed_time(e[4]))
     return out
 
 
@@ -369,7 +379,11 @@ def run_ours(args):
     step_max_ms, _ = aggregate(step_ms_total, 0.0)
     value = flops_all / (bwd_max_ms * 1e-3) / 1e12
 
-    main_ms = statistics.mean(res["main"])
+    # Per-kernel times from a pass of the same steps with events between the
+    # backward kernels (which the timed steps leave out, see time_workload).
+    brk_steps = max(20, min(args.steps, 200))
+    brk = time_workload(w, brk_steps, 3, flush, split=True)
+    main_ms = statistics.mean(brk["main"])
     achieved = w.bwd_flops() / (main_ms * 1e-3) / 1e12
 
     e2e_steps = max(10, min(args.steps, 200))
@@ -381,13 +395,14 @@ def run_ours(args):
     if not args.no_extra:
         extra = {}
         for name in D128:
-            r = time_workload(WORKLOADS[name], 10, 3, flush)
+            r = time_workload(WORKLOADS[name], 10, 3, flush, split=True)
+            rw = time_workload(WORKLOADS[name], 10, 3, flush)
             mm = statistics.median(r["main"])
             extra[name] = {
                 "bwd_main_tflops": round(WORKLOADS[name].bwd_flops() / mm / 1e9, 1),
                 "bwd_main_frac": round(WORKLOADS[name].bwd_flops() / mm / 1e9 / peak_tf, 4),
                 "bwd_total_tflops": round(WORKLOADS[name].bwd_flops()
-                                          / statistics.median(r["bwd"]) / 1e9, 1),
+                                          / statistics.median(rw["bwd"]) / 1e9, 1),
                 "fwd_tflops": round(WORKLOADS[name].fwd_flops()
                                     / statistics.median(r["fwd"]) / 1e9, 1),
                 "main_ms_median": round(mm, 4),
@@ -411,8 +426,10 @@ def run_ours(args):
         "config": {
             "workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
             "scale": "1/sqrt(d)", "l2": "flushed before every step (512 MiB write)",
-            "timing": "CUDA events per step on the launching stream; value = backward FLOPs "
-                      "(10*B*H*N^2*d, halved causal) / attn_bwd device time",
+            "timing": "CUDA events per step on the launching stream, around the forward and "
+                      "around the whole attn_bwd call (no events between its three kernels, "
+                      "which start early by programmatic dependent launch); value = backward "
+                      "FLOPs (10*B*H*N^2*d, halved causal) / attn_bwd device time",
             "parallelism": "replicas (independent heads), no collective on the data path",
         },
         "fwd_tflops": round(w.fwd_flops() / statistics.mean(res["fwd"]) / 1e9, 2),
@@ -420,6 +437,14 @@ def run_ours(args):
         "fwd_ms": round(sum(res["fwd"]) / args.steps, 5),
         "bwd_fwd_time_ratio": round(sum(res["bwd"]) / max(sum(res["fwd"]), 1e-9), 3),
         "wall_s_timed_region": round(wall_s, 3),
+        "bwd_kernels_ms": {
+            "preprocess": round(statistics.mean(brk["prep"]), 5),
+            "main": round(main_ms, 5),
+            "dq_convert": round(statistics.mean(brk["conv"]), 5),
+            "sum_with_events_between": round(statistics.mean(brk["bwd"]), 5),
+            "steps": brk_steps,
+            "what": "a pass of the same steps after the timed region, with an event between "
+                    "each backward kernel (this disables their early start)"},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5), "steps": e2e_steps,
@@ -437,6 +462,8 @@ def run_ours(args):
                            % ("of measured" if peak_src == "measured" else "of fallback"),
             "flops_per_launch": w.bwd_flops(),
             "avg_launch_ms": round(main_ms, 5),
+            "launch_timing": "CUDA events around each main-kernel launch, %d steps of the same "
+                             "workload run right after the timed region" % brk_steps,
         },
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,

@@ -35,7 +35,10 @@
  * alive and unmodified, and outputs untouched, until the stream reaches the
  * call.  Kernels never trap: a device-side failure (a bounded wait that ran
  * out) is recorded in a per-device error word that attn_last_device_error()
- * reads.
+ * reads.  Every kernel is launched with programmatic dependent launch
+ * allowed: it may start its set-up while the previous kernel in the stream
+ * is finishing, and waits for that kernel to complete (griddepcontrol.wait)
+ * before it reads global memory, so stream order is kept for all data.
  */
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
