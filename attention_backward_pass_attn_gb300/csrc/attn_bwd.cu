@@ -744,8 +744,7 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  cudaStream_t stream) {
   using Ly = Layout<HD>;
   auto kern = attn_bwd_main_kernel<HD, CAUSAL>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  cudaError_t e = set_smem_limit_once<attn_bwd_main_kernel<HD, CAUSAL>>(Ly::kBytes);
   if (e != cudaSuccess) return e;
   // Persistent grid: at most one CTA per SM, each walking its work items.
   const long long n_items = (long long)s.n_tiles * s.BH;

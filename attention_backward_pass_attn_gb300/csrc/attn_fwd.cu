@@ -367,7 +367,7 @@ static cudaError_t launch_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             float scale, int* err, cudaStream_t stream) {
   using Ly = Layout<HD>;
   auto kern = attn_fwd_kernel<HD, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  cudaError_t e = set_smem_limit_once<attn_fwd_kernel<HD, CAUSAL>>(Ly::kBytes);
   if (e != cudaSuccess) return e;
   const int n_pairs = (s.n_tiles + 1) / 2;
   const dim3 grid(unsigned(n_pairs) * unsigned(s.BH));
