@@ -74,15 +74,29 @@ constexpr int kBarDrain = 21;
 constexpr int kNumBars = 22;
 constexpr int kDrainBarrierId = 1;  // named barrier of the 128 dQ-drain threads
 
-// Work items are (head, key/value tile) pairs with index i = jt * BH + bh.
-// Under the causal mask a smaller jt sees more query tiles, so index order is
-// heaviest first.  The grid is persistent (at most one CTA per SM); CTA b of G
-// takes items b, 2G-1-b, 2G+b, 4G-1-b, ... (a snake over rounds, which evens
-// out the heavy-first order).  Returns -1 past the last item.
+// Work items are (head, key/value tile) pairs.  Heads are taken in groups
+// of HG whose query, dO and dQ-accumulator tiles fit in L2 together; within
+// a group the index runs key/value-tile major, i = jt * hg + (bh - first
+// head), so under the causal mask (a smaller jt sees more query tiles) each
+// group goes heaviest first.  The grid is persistent (at most one CTA per
+// SM); CTA b of G takes items b, 2G-1-b, 2G+b, 4G-1-b, ... (a snake over
+// rounds, which evens out the heavy-first order).  Returns -1 past the last
+// item.
 __device__ __forceinline__ int snake_item(int k, int b, int G, int n_items) {
   const int idx = (k & 1) ? k * G + (G - 1 - b) : k * G + b;
   return idx < n_items ? idx : -1;
 }
+
+struct ItemMap {
+  int BH, n_tiles, HG;
+  __device__ __forceinline__ void decode(int i, int& jt, int& bh) const {
+    const int per_group = HG * n_tiles;
+    const int gr = i / per_group, r = i - gr * per_group;
+    const int hg = BH - gr * HG < HG ? BH - gr * HG : HG;  // heads in this group
+    jt = r / hg;
+    bh = gr * HG + (r - jt * hg);
+  }
+};
 
 template <int HD>
 struct Layout {
@@ -129,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmAcc, const float* __restrict__ L2ws,
                          const float* __restrict__ Dws,
                          __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int BH,
-                         int N, float scale, float scale_log2, int* err) {
+                         int N, int head_group, float scale, float scale_log2, int* err) {
   using Ly = Layout<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -143,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (N + 127) >> 7;
   const int Npad = n_tiles * 128;
   const int n_items = BH * n_tiles;
+  const ItemMap imap{BH, n_tiles, head_group};
   const int G = gridDim.x, b = blockIdx.x;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
@@ -205,9 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
-      const int jt = item / BH, bh = item % BH;
+      int jt, bh;
+      imap.decode(item, jt, bh);
       const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
       const int next = snake_item(k + 1, b, G, n_items);
+      int njt = 0, nbh = 0;
+      if (next >= 0) imap.decode(next, njt, nbh);
       if (k > 0 && !(ok = mbar_wait_warp(bar(kBarVEmpty), (k - 1) & 1, ctx, 0x212))) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar(kBarVFull), Ly::kTileBytes);
@@ -227,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is often a cold region, and its first tiles are needed right at the
         // item switch.
         if (next >= 0) {
-          const int njt = next / BH, nbh = next % BH, nq = CAUSAL ? njt : 0;
+          const int nq = CAUSAL ? njt : 0;
 #pragma unroll
           for (int cb = 0; cb < HD / 64; ++cb) {
             tma_prefetch_3d(&tmK, cb * 64, njt * 128, nbh);
@@ -257,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int qbh = bh, qt = it0 + it + 1;
         if (it + 1 == n_it) {
           if (next < 0) continue;
-          qbh = next % BH;
-          qt = CAUSAL ? next / BH : 0;
+          qbh = nbh;
+          qt = CAUSAL ? njt : 0;
         }
         const int gn = g + 1;
         if (gn >= 2 &&
@@ -303,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
-      const int jt = item / BH;
+      int jt, bh_unused;
+      imap.decode(item, jt, bh_unused);
       const int n_it = n_tiles - (CAUSAL ? jt : 0);
       if (!(ok = mbar_wait_warp(bar(kBarKFull), k & 1, ctx, 0x220))) break;
       if (!(ok = mbar_wait_warp(bar(kBarQFull + (g & 1)), (g >> 1) & 1, ctx, 0x221))) break;
@@ -415,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
-      const int jt = item / BH, bh = item % BH;
+      int jt, bh;
+      imap.decode(item, jt, bh);
       const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
       for (int it = 0; it < n_it; ++it, ++g) {
         const int s = g & 1, qt = it0 + it;
@@ -533,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
-      const int jt = item / BH, bh = item % BH;
+      int jt, bh;
+      imap.decode(item, jt, bh);
       const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
       for (int it = 0; it < n_it; ++it, ++g) {
         const int qt = it0 + it;
@@ -736,6 +757,35 @@ static int num_sms() {
   return cached[dev];
 }
 
+// L2 size of the current device in bytes (cached per device).
+static size_t l2_bytes() {
+  static size_t cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return size_t(32) << 20;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0)
+      n = 32 << 20;
+    cached[dev] = size_t(n);
+  }
+  return cached[dev];
+}
+
+// Heads per work-item group: as many as keep the group's Q, dO (bf16) and
+// dQ accumulator (fp32), 8 bytes per element of a head, within half the L2.
+// Without the mask every item of a head walks all its query tiles, so
+// grouping turns most Q/dO reads into L2 hits (measured +13% at N = 8192,
+// d = 128).  Under the causal mask, grouping measured slower (-4 to -9%):
+// all heads form one group there, and the order stays heaviest first.
+static int head_group(const Shape& s) {
+  if (s.causal) return s.BH;
+  const size_t per_head = size_t(s.Npad) * s.d * 8;
+  size_t hg = (l2_bytes() / 2) / per_head;
+  if (hg < 1) hg = 1;
+  if (hg > size_t(s.BH)) hg = size_t(s.BH);
+  return int(hg);
+}
+
 template <int HD, bool CAUSAL>
 static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO,
@@ -751,7 +801,7 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   const dim3 grid(unsigned(n_items < num_sms() ? n_items : num_sms()));
   return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV, tmdO, tmAcc,
                        ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
-                       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, scale,
+                       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, head_group(s), scale,
                        scale * 1.4426950408889634f, err);
 }
 
