@@ -89,8 +89,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_tiles = (N + 127) >> 7;
   const int n_pairs = (n_tiles + 1) >> 1;
-  const int bh = blockIdx.x % BH;
-  const int pair = CAUSAL ? (n_pairs - 1 - int(blockIdx.x / BH)) : int(blockIdx.x / BH);
+  // Causal: pairs of query tiles heaviest first (a later pair sees more
+  // key/value tiles), across all heads.  Without the mask every pair costs
+  // the same: CTAs run head by head, so the CTAs resident at one time share
+  // their heads' K and V in L2.
+  const int bh = CAUSAL ? int(blockIdx.x % BH) : int(blockIdx.x / n_pairs);
+  const int pair = CAUSAL ? (n_pairs - 1 - int(blockIdx.x / BH)) : int(blockIdx.x % n_pairs);
   const int qt_a = 2 * pair;
   const bool has_b = qt_a + 1 < n_tiles;
   const int n_kv = CAUSAL ? min(n_tiles, qt_a + (has_b ? 2 : 1)) : n_tiles;
