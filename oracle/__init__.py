@@ -68,15 +68,15 @@ def load(path: str | None = None):
         lib = ctypes.CDLL(lib_path)
         dp = ctypes.POINTER(ctypes.c_double)
         L = ctypes.c_long
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, L, L, L, ctypes.c_int,
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, L, L, L, ctypes.c_int, L,
                                         ctypes.c_double, dp, dp, ctypes.c_int]
         lib.oracle_attn_fwd.restype = ctypes.c_int
-        lib.oracle_attn_fwd_bwd.argtypes = [dp, dp, dp, dp, L, L, L, ctypes.c_int,
+        lib.oracle_attn_fwd_bwd.argtypes = [dp, dp, dp, dp, L, L, L, ctypes.c_int, L,
                                             ctypes.c_double, dp, dp, dp, dp, dp,
                                             dp, ctypes.c_int]
         lib.oracle_attn_fwd_bwd.restype = ctypes.c_int
         lp = ctypes.POINTER(ctypes.c_long)
-        lib.oracle_attn_head_rows.argtypes = [dp, dp, dp, dp, L, L, ctypes.c_int,
+        lib.oracle_attn_head_rows.argtypes = [dp, dp, dp, dp, L, L, ctypes.c_int, L,
                                               ctypes.c_double, L, lp, L, lp, dp, dp, dp,
                                               dp, dp, ctypes.c_int]
         lib.oracle_attn_head_rows.restype = ctypes.c_int
@@ -105,8 +105,11 @@ def max_threads(lib=None) -> int:
     return int((lib or load()).oracle_max_threads())
 
 
-def attention_forward(q, k, v, causal: bool, scale: float, threads: int = 0, lib=None):
-    """O [B,H,N,d] and L [B,H,N] (natural-log log-sum-exp), both float64."""
+def attention_forward(q, k, v, causal: bool, scale: float, threads: int = 0, lib=None,
+                      window: int = 0):
+    """O [B,H,N,d] and L [B,H,N] (natural-log log-sum-exp), both float64.
+
+    window > 0 (causal only): query i sees keys i - window < j <= i."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     if q.ndim != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must share the shape [B, H, N, d]")
@@ -114,7 +117,7 @@ def attention_forward(q, k, v, causal: bool, scale: float, threads: int = 0, lib
     o = np.zeros_like(q)
     lse = np.zeros((B, H, N), dtype=np.float64)
     st = (lib or load()).oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B * H, N, d,
-                                         int(bool(causal)), float(scale), _ptr(o),
+                                         int(bool(causal)), int(window), float(scale), _ptr(o),
                                          _ptr(lse), int(threads))
     if st != 0:
         raise RuntimeError("oracle_attn_fwd failed with status %d" % st)
@@ -122,7 +125,7 @@ def attention_forward(q, k, v, causal: bool, scale: float, threads: int = 0, lib
 
 
 def attention_forward_backward(q, k, v, do, causal: bool, scale: float,
-                               threads: int = 0, lib=None) -> dict:
+                               threads: int = 0, lib=None, window: int = 0) -> dict:
     """Exact forward and analytic backward in float64.
 
     Returns a dict with O, L, D (= rowsum(dO * O)), dQ, dK, dV.
@@ -135,7 +138,7 @@ def attention_forward_backward(q, k, v, do, causal: bool, scale: float,
     out["L"] = np.zeros((B, H, N), dtype=np.float64)
     out["D"] = np.zeros((B, H, N), dtype=np.float64)
     st = (lib or load()).oracle_attn_fwd_bwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, N, d, int(bool(causal)),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, N, d, int(bool(causal)), int(window),
         float(scale), _ptr(out["O"]), _ptr(out["L"]), _ptr(out["D"]),
         _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), int(threads))
     if st != 0:
@@ -144,7 +147,7 @@ def attention_forward_backward(q, k, v, do, causal: bool, scale: float,
 
 
 def attention_head_rows(q, k, v, do, causal: bool, scale: float, q_rows, k_rows,
-                        threads: int = 0, lib=None) -> dict:
+                        threads: int = 0, lib=None, window: int = 0) -> dict:
     """Sampled rows of one head ([N, d] inputs), for shapes too large to do in full.
 
     Returns O, L, dQ at the query rows ``q_rows`` and dK, dV at the key rows
@@ -161,7 +164,8 @@ def attention_head_rows(q, k, v, do, causal: bool, scale: float, q_rows, k_rows,
            "dK": np.zeros((len(kr), d)), "dV": np.zeros((len(kr), d))}
     lp = ctypes.POINTER(ctypes.c_long)
     st = (lib or load()).oracle_attn_head_rows(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, d, int(bool(causal)), float(scale),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, d, int(bool(causal)), int(window),
+        float(scale),
         len(qr), qr.ctypes.data_as(lp), len(kr), kr.ctypes.data_as(lp), _ptr(out["O"]),
         _ptr(out["L"]), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), int(threads))
     if st != 0:

@@ -33,6 +33,12 @@
  * mask of 50% density).  Every row keeps at least its diagonal entry, so no
  * row is empty.
  *
+ * Sliding window.  With causal and a window W > 0, key j is visible to query
+ * i when i - W < j <= i: each query sees itself and the W - 1 keys before it
+ * (the banded causal mask of sliding-window attention, named in "Training -
+ * CUDA Moat Still Alive", section on attention variants, as the Mistral 7B
+ * mask).  M_ij = -inf outside the band; W >= N is the plain causal mask.
+ *
  * How.  Three passes over the rows of each head, each a direct evaluation of
  * the definition above, all in double precision:
  *   pass 1, over query rows i:   L_i, O_i, D_i
@@ -65,16 +71,23 @@ static double dot(const double *a, const double *b, long d) {
   return acc;
 }
 
-/* Number of keys row i may attend to. */
+/* One past the last key row i may attend to. */
 static long row_len(long i, long N, int causal) { return causal ? i + 1 : N; }
 
-/* Fill srow[j] = scale * <q_i, k_j> for the unmasked keys j of row i and
- * return how many there are. */
+/* The first key row i may attend to: under a sliding window W, i - W + 1. */
+static long row_start(long i, int causal, long window) {
+  return (causal && window > 0 && i - window + 1 > 0) ? i - window + 1 : 0;
+}
+
+/* Fill srow[j] = scale * <q_i, k_j> for the unmasked keys j of row i, which
+ * are lo <= j < n; set *lo and return n. */
 static long scores_row(const double *Qh, const double *Kh, long i, long N,
-                       long d, int causal, double scale, double *srow) {
+                       long d, int causal, long window, double scale, double *srow,
+                       long *lo) {
   long n = row_len(i, N, causal);
   const double *qi = Qh + i * d;
-  for (long j = 0; j < n; ++j) srow[j] = scale * dot(qi, Kh + j * d, d);
+  *lo = row_start(i, causal, window);
+  for (long j = *lo; j < n; ++j) srow[j] = scale * dot(qi, Kh + j * d, d);
   return n;
 }
 
@@ -89,18 +102,19 @@ static void set_threads(int nthreads) {
 /* L_i, O_i and (when dOh is given) D_i = <dO_i, O_i> for one query row i of
  * one head. */
 static void fwd_row(const double *Qh, const double *Kh, const double *Vh,
-                    const double *dOh, long N, long d, int causal, double scale,
-                    long i, double *srow, double *Li_out, double *Oi,
+                    const double *dOh, long N, long d, int causal, long window,
+                    double scale, long i, double *srow, double *Li_out, double *Oi,
                     double *Di_out) {
-  long n = scores_row(Qh, Kh, i, N, d, causal, scale, srow);
+  long lo;
+  long n = scores_row(Qh, Kh, i, N, d, causal, window, scale, srow, &lo);
   double m = -INFINITY;
-  for (long j = 0; j < n; ++j) m = srow[j] > m ? srow[j] : m;
+  for (long j = lo; j < n; ++j) m = srow[j] > m ? srow[j] : m;
   double l = 0.0;
-  for (long j = 0; j < n; ++j) l += exp(srow[j] - m);
+  for (long j = lo; j < n; ++j) l += exp(srow[j] - m);
   double Li = m + log(l);
   *Li_out = Li;
   for (long c = 0; c < d; ++c) Oi[c] = 0.0;
-  for (long j = 0; j < n; ++j) {
+  for (long j = lo; j < n; ++j) {
     double p = exp(srow[j] - Li);
     const double *vj = Vh + j * d;
     for (long c = 0; c < d; ++c) Oi[c] += p * vj[c];
@@ -111,7 +125,7 @@ static void fwd_row(const double *Qh, const double *Kh, const double *Vh,
 /* Pass 1: L, O and D for every query row. */
 static int pass_forward(const double *Q, const double *K, const double *V,
                         const double *dO, long BH, long N, long d, int causal,
-                        double scale, double *O, double *L, double *D) {
+                        long window, double scale, double *O, double *L, double *D) {
   int failed = 0;
 #pragma omp parallel
   {
@@ -125,7 +139,7 @@ static int pass_forward(const double *Q, const double *K, const double *V,
       for (long i = 0; i < N; ++i) {
         if (!srow) continue;
         fwd_row(Q + h * N * d, K + h * N * d, V + h * N * d,
-                dO ? dO + h * N * d : NULL, N, d, causal, scale, i, srow,
+                dO ? dO + h * N * d : NULL, N, d, causal, window, scale, i, srow,
                 L + h * N + i, O + (h * N + i) * d, D ? D + h * N + i : NULL);
       }
     }
@@ -137,11 +151,13 @@ static int pass_forward(const double *Q, const double *K, const double *V,
 /* dQ_i = s * sum_j P_ij (dP_ij - D_i) k_j for one query row i of one head. */
 static void dq_row(const double *Qh, const double *Kh, const double *Vh,
                    const double *dOh, double Li, double Di, long N, long d,
-                   int causal, double scale, long i, double *srow, double *dQi) {
+                   int causal, long window, double scale, long i, double *srow,
+                   double *dQi) {
   const double *dOi = dOh + i * d;
-  long n = scores_row(Qh, Kh, i, N, d, causal, scale, srow);
+  long lo;
+  long n = scores_row(Qh, Kh, i, N, d, causal, window, scale, srow, &lo);
   for (long c = 0; c < d; ++c) dQi[c] = 0.0;
-  for (long j = 0; j < n; ++j) {
+  for (long j = lo; j < n; ++j) {
     double p = exp(srow[j] - Li);
     double dp = dot(dOi, Vh + j * d, d);
     double ds = p * (dp - Di);
@@ -152,15 +168,17 @@ static void dq_row(const double *Qh, const double *Kh, const double *Vh,
 }
 
 /* dK_j = s * sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i for one key row j of
- * one head.  Under the causal mask, key j is seen by query rows i >= j only. */
+ * one head.  Under the causal mask, key j is seen by query rows i >= j only;
+ * under a sliding window W also only by rows i < j + W. */
 static void dkdv_row(const double *Qh, const double *Kh, const double *Vh,
                      const double *dOh, const double *Lh, const double *Dh, long N,
-                     long d, int causal, double scale, long j, double *dKj,
-                     double *dVj) {
+                     long d, int causal, long window, double scale, long j,
+                     double *dKj, double *dVj) {
   const double *kj = Kh + j * d, *vj = Vh + j * d;
   for (long c = 0; c < d; ++c) dKj[c] = dVj[c] = 0.0;
   long i0 = causal ? j : 0;
-  for (long i = i0; i < N; ++i) {
+  long i1 = (causal && window > 0 && j + window < N) ? j + window : N;
+  for (long i = i0; i < i1; ++i) {
     const double *qi = Qh + i * d, *dOi = dOh + i * d;
     double sij = scale * dot(qi, kj, d);
     double p = exp(sij - Lh[i]);
@@ -177,7 +195,7 @@ static void dkdv_row(const double *Qh, const double *Kh, const double *Vh,
 /* Pass 2: dQ for every query row. */
 static int pass_dq(const double *Q, const double *K, const double *V,
                    const double *dO, const double *L, const double *D, long BH,
-                   long N, long d, int causal, double scale, double *dQ) {
+                   long N, long d, int causal, long window, double scale, double *dQ) {
   int failed = 0;
 #pragma omp parallel
   {
@@ -191,7 +209,7 @@ static int pass_dq(const double *Q, const double *K, const double *V,
       for (long i = 0; i < N; ++i) {
         if (!srow) continue;
         dq_row(Q + h * N * d, K + h * N * d, V + h * N * d, dO + h * N * d,
-               L[h * N + i], D[h * N + i], N, d, causal, scale, i, srow,
+               L[h * N + i], D[h * N + i], N, d, causal, window, scale, i, srow,
                dQ + (h * N + i) * d);
       }
     }
@@ -203,13 +221,13 @@ static int pass_dq(const double *Q, const double *K, const double *V,
 /* Pass 3: dK and dV for every key row. */
 static int pass_dkdv(const double *Q, const double *K, const double *V,
                      const double *dO, const double *L, const double *D,
-                     long BH, long N, long d, int causal, double scale,
+                     long BH, long N, long d, int causal, long window, double scale,
                      double *dK, double *dV) {
 #pragma omp parallel for collapse(2) schedule(dynamic, 16)
   for (long h = 0; h < BH; ++h) {
     for (long j = 0; j < N; ++j) {
       dkdv_row(Q + h * N * d, K + h * N * d, V + h * N * d, dO + h * N * d,
-               L + h * N, D + h * N, N, d, causal, scale, j,
+               L + h * N, D + h * N, N, d, causal, window, scale, j,
                dK + (h * N + j) * d, dV + (h * N + j) * d);
     }
   }
@@ -217,8 +235,9 @@ static int pass_dkdv(const double *Q, const double *K, const double *V,
 }
 
 static int check_args(const void *a, const void *b, const void *c, long BH,
-                      long N, long d, double scale) {
+                      long N, long d, int causal, long window, double scale) {
   if (BH < 0 || N < 0 || d < 0) return ORACLE_ERR_ARG;
+  if (window < 0 || (window > 0 && !causal)) return ORACLE_ERR_ARG; /* the band is causal */
   if (BH * N * d > 0 && (!a || !b || !c)) return ORACLE_ERR_ARG;
   if (!(scale == scale)) return ORACLE_ERR_ARG; /* NaN */
   return ORACLE_OK;
@@ -226,31 +245,31 @@ static int check_args(const void *a, const void *b, const void *c, long BH,
 
 /* Forward only: O [BH][N][d] and L [BH][N]. */
 int oracle_attn_fwd(const double *Q, const double *K, const double *V, long BH,
-                    long N, long d, int causal, double scale, double *O,
+                    long N, long d, int causal, long window, double scale, double *O,
                     double *L, int nthreads) {
-  int st = check_args(Q, K, V, BH, N, d, scale);
+  int st = check_args(Q, K, V, BH, N, d, causal, window, scale);
   if (st) return st;
   if (BH * N == 0) return ORACLE_OK;
   if (!O || !L) return ORACLE_ERR_ARG;
   set_threads(nthreads);
-  return pass_forward(Q, K, V, NULL, BH, N, d, causal, scale, O, L, NULL);
+  return pass_forward(Q, K, V, NULL, BH, N, d, causal, window, scale, O, L, NULL);
 }
 
 /* Forward and backward: O, L, D = rowsum(dO * O), dQ, dK, dV. */
 int oracle_attn_fwd_bwd(const double *Q, const double *K, const double *V,
                         const double *dO, long BH, long N, long d, int causal,
-                        double scale, double *O, double *L, double *D,
+                        long window, double scale, double *O, double *L, double *D,
                         double *dQ, double *dK, double *dV, int nthreads) {
-  int st = check_args(Q, K, V, BH, N, d, scale);
+  int st = check_args(Q, K, V, BH, N, d, causal, window, scale);
   if (st) return st;
   if (BH * N == 0) return ORACLE_OK;
   if (!dO || !O || !L || !D || !dQ || !dK || !dV) return ORACLE_ERR_ARG;
   set_threads(nthreads);
-  st = pass_forward(Q, K, V, dO, BH, N, d, causal, scale, O, L, D);
+  st = pass_forward(Q, K, V, dO, BH, N, d, causal, window, scale, O, L, D);
   if (st) return st;
-  st = pass_dq(Q, K, V, dO, L, D, BH, N, d, causal, scale, dQ);
+  st = pass_dq(Q, K, V, dO, L, D, BH, N, d, causal, window, scale, dQ);
   if (st) return st;
-  return pass_dkdv(Q, K, V, dO, L, D, BH, N, d, causal, scale, dK, dV);
+  return pass_dkdv(Q, K, V, dO, L, D, BH, N, d, causal, window, scale, dK, dV);
 }
 
 /* Threads the oracle would use (1 without OpenMP). */
@@ -268,12 +287,12 @@ int oracle_max_threads(void) {
  * and key rows krows[0..nk).  Outputs: O_rows, dQ_rows [nq][d], L_rows [nq],
  * dK_rows, dV_rows [nk][d].  Q, K, V, dO are one head, [N][d]. */
 int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
-                          const double *dO, long N, long d, int causal,
+                          const double *dO, long N, long d, int causal, long window,
                           double scale, long nq, const long *qrows, long nk,
                           const long *krows, double *O_rows, double *L_rows,
                           double *dQ_rows, double *dK_rows, double *dV_rows,
                           int nthreads) {
-  int st = check_args(Q, K, V, 1, N, d, scale);
+  int st = check_args(Q, K, V, 1, N, d, causal, window, scale);
   if (st) return st;
   if (nq < 0 || nk < 0 || (nq && (!qrows || !O_rows || !L_rows || !dQ_rows)) ||
       (nk && (!krows || !dK_rows || !dV_rows)) || !dO)
@@ -299,9 +318,10 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
       for (long t = 0; t < nq; ++t) {
         if (!srow) continue;
         long i = qrows[t];
-        fwd_row(Q, K, V, dO, N, d, causal, scale, i, srow, &Li, O_rows + t * d, &Di);
+        fwd_row(Q, K, V, dO, N, d, causal, window, scale, i, srow, &Li, O_rows + t * d,
+                &Di);
         L_rows[t] = Li;
-        dq_row(Q, K, V, dO, Li, Di, N, d, causal, scale, i, srow, dQ_rows + t * d);
+        dq_row(Q, K, V, dO, Li, Di, N, d, causal, window, scale, i, srow, dQ_rows + t * d);
       }
       free(srow);
     }
@@ -314,7 +334,7 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
     free(O); free(L); free(D);
     return ORACLE_ERR_NOMEM;
   }
-  st = pass_forward(Q, K, V, dO, 1, N, d, causal, scale, O, L, D);
+  st = pass_forward(Q, K, V, dO, 1, N, d, causal, window, scale, O, L, D);
   if (!st) {
     int failed = 0;
 #pragma omp parallel
@@ -330,12 +350,13 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
         long i = qrows[t];
         memcpy(O_rows + t * d, O + i * d, sizeof(double) * (size_t)d);
         L_rows[t] = L[i];
-        dq_row(Q, K, V, dO, L[i], D[i], N, d, causal, scale, i, srow, dQ_rows + t * d);
+        dq_row(Q, K, V, dO, L[i], D[i], N, d, causal, window, scale, i, srow,
+               dQ_rows + t * d);
       }
 #pragma omp for schedule(dynamic, 1)
       for (long t = 0; t < nk; ++t)
-        dkdv_row(Q, K, V, dO, L, D, N, d, causal, scale, krows[t], dK_rows + t * d,
-                 dV_rows + t * d);
+        dkdv_row(Q, K, V, dO, L, D, N, d, causal, window, scale, krows[t],
+                 dK_rows + t * d, dV_rows + t * d);
       free(srow);
     }
     if (failed) st = ORACLE_ERR_NOMEM;

@@ -13,6 +13,11 @@ AssertionError when the oracle disagrees with:
   routine, used as a cross-check only),
 * a pure-Python brute force over the full N x N matrices for N <= 8.
 
+The sliding-window (banded causal) mask -- key j visible to query i when
+i - W < j <= i -- has pins of its own: finite differences, the closed forms
+W = 1 and W >= N, truncation to the window's keys, the brute force with the
+band, and PyTorch with an explicit band mask.
+
 The method is exact attention as named by "Training Transformers and Hybrid
 models on AMD Instinct MI300X Accelerators", section "Flash Attention"; the
 pages print no worked example, so every pin is mathematical.
@@ -31,8 +36,9 @@ def _rand(rng, shape, std=1.0):
     return rng.standard_normal(shape) * std
 
 
-def _fb(lib, q, k, v, do, causal, scale):
-    return oracle.attention_forward_backward(q, k, v, do, causal, scale, lib=lib)
+def _fb(lib, q, k, v, do, causal, scale, window=0):
+    return oracle.attention_forward_backward(q, k, v, do, causal, scale, lib=lib,
+                                             window=window)
 
 
 def _close(a, b, rtol, atol=0.0, what=""):
@@ -219,9 +225,15 @@ def pin_permutation(lib):
 # --------------------------------------------------------------------------
 # Brute force over the full matrices, pure Python loops, tiny N.
 # --------------------------------------------------------------------------
-def _brute(q, k, v, do, causal, s):
+def _brute(q, k, v, do, causal, s, window=0):
     N, d = len(q), len(q[0])
-    S = [[(s * sum(q[i][c] * k[j][c] for c in range(d)) if (not causal or j <= i)
+
+    def visible(i, j):
+        if not causal:
+            return True
+        return j <= i and (window == 0 or i - j < window)
+
+    S = [[(s * sum(q[i][c] * k[j][c] for c in range(d)) if visible(i, j)
            else -math.inf) for j in range(N)] for i in range(N)]
     L = []
     for i in range(N):
@@ -314,6 +326,106 @@ def pin_row_sampler_matches_full(lib):
         assert np.array_equal(qonly["L"], full["L"][0, 0][qr])
 
 
+# --------------------------------------------------------------------------
+# Sliding window (banded causal mask).
+# --------------------------------------------------------------------------
+def pin_window_finite_differences(lib):
+    rng = np.random.default_rng(21)
+    for (N, d, W) in ((5, 2, 2), (7, 3, 3), (6, 2, 1)):
+        q, k, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(4))
+        scale = 0.9
+        out = _fb(lib, q, k, v, do, True, scale, window=W)
+
+        def loss(q_, k_, v_):
+            o, _ = oracle.attention_forward(q_, k_, v_, True, scale, lib=lib, window=W)
+            return float(np.sum(do * o))
+
+        h = 1e-6
+        for pos, name in enumerate(("dQ", "dK", "dV")):
+            x = (q, k, v)[pos]
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp = x.copy(); xp[idx] += h
+                xm = x.copy(); xm[idx] -= h
+                args_p = [q, k, v]; args_m = [q, k, v]
+                args_p[pos] = xp; args_m[pos] = xm
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            _close(out[name], num, rtol=1e-6, atol=1e-8,
+                   what="window finite differences %s N=%d W=%d" % (name, N, W))
+
+
+def pin_window_closed_forms(lib):
+    """W >= N is the plain causal mask (bit for bit); W = 1 leaves each query
+    only itself: P = 1, so O = V, L_i = s<q_i,k_i>, dV = dO and dS = 0, hence
+    dQ = dK = 0 exactly."""
+    rng = np.random.default_rng(22)
+    N, d, s = 19, 4, 0.45
+    q, k, v, do = (_rand(rng, (1, 2, N, d)) for _ in range(4))
+    causal = _fb(lib, q, k, v, do, True, s)
+    for W in (N, N + 5, 1000):
+        wide = _fb(lib, q, k, v, do, True, s, window=W)
+        for name in causal:
+            assert np.array_equal(wide[name], causal[name]), "W=%d %s" % (W, name)
+    one = _fb(lib, q, k, v, do, True, s, window=1)
+    assert np.array_equal(one["O"], v), "W=1: O = V"
+    _close(one["L"], s * np.sum(q * k, axis=-1), 1e-14, what="W=1: L")
+    assert np.array_equal(one["dV"], do), "W=1: dV = dO"
+    assert not np.any(one["dQ"]) and not np.any(one["dK"]), "W=1: dQ = dK = 0"
+
+
+def pin_window_truncation(lib):
+    """Query i under a window W attends exactly to keys i-W+1 .. i: its O, L
+    and dQ equal those of unmasked attention of q_i over that slice alone."""
+    rng = np.random.default_rng(23)
+    N, d, W, s = 40, 5, 7, 0.5
+    q, k, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(4))
+    out = _fb(lib, q, k, v, do, True, s, window=W)
+    for i in (0, 3, 6, 7, 20, 39):
+        lo = max(0, i - W + 1)
+        n = i + 1 - lo
+        qi = np.repeat(q[:, :, i:i + 1], n, axis=2)
+        doi = np.repeat(do[:, :, i:i + 1], n, axis=2)
+        part = _fb(lib, qi, k[:, :, lo:i + 1], v[:, :, lo:i + 1], doi, False, s)
+        _close(out["O"][0, 0, i], part["O"][0, 0, 0], 1e-13, what="trunc O row %d" % i)
+        _close(out["L"][0, 0, i], part["L"][0, 0, 0], 1e-13, what="trunc L row %d" % i)
+        _close(out["dQ"][0, 0, i], part["dQ"][0, 0, 0], 1e-12, what="trunc dQ row %d" % i)
+
+
+def pin_window_brute_force(lib):
+    rng = np.random.default_rng(24)
+    for N, d, W in ((5, 2, 2), (8, 3, 3), (8, 2, 5)):
+        q, k, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(4))
+        s = 0.8
+        out = _fb(lib, q, k, v, do, True, s, window=W)
+        ref = _brute(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(),
+                     do[0, 0].tolist(), True, s, window=W)
+        for name in ("O", "dQ", "dK", "dV", "L", "D"):
+            _close(out[name][0, 0], np.array(ref[name]), 1e-12,
+                   what="window brute %s N=%d W=%d" % (name, N, W))
+
+
+def pin_window_torch_fp64(lib):
+    import torch
+
+    rng = np.random.default_rng(25)
+    for (N, d, W) in ((64, 16, 16), (131, 8, 50), (300, 32, 129)):
+        q, k, v, do = (_rand(rng, (1, 2, N, d)) for _ in range(4))
+        s = 1.0 / math.sqrt(d)
+        out = _fb(lib, q, k, v, do, True, s, window=W)
+        i = torch.arange(N).view(N, 1)
+        j = torch.arange(N).view(1, N)
+        band = (j <= i) & (i - j < W)  # True = attend
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True)
+                      for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=band,
+                                                              scale=s)
+        to.backward(torch.tensor(do, dtype=torch.float64))
+        _close(out["O"], to.detach().numpy(), 1e-11, what="window torch O")
+        _close(out["dQ"], tq.grad.numpy(), 1e-10, what="window torch dQ")
+        _close(out["dK"], tk.grad.numpy(), 1e-10, what="window torch dK")
+        _close(out["dV"], tv.grad.numpy(), 1e-10, what="window torch dV")
+
+
 ALL_PINS = [
     pin_finite_differences,
     pin_single_key,
@@ -325,4 +437,9 @@ ALL_PINS = [
     pin_brute_force,
     pin_torch_fp64,
     pin_row_sampler_matches_full,
+    pin_window_finite_differences,
+    pin_window_closed_forms,
+    pin_window_truncation,
+    pin_window_brute_force,
+    pin_window_torch_fp64,
 ]
