@@ -54,8 +54,11 @@ def load_library(path: str | None = None):
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         sig = {
             "attn_fwd": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]),
+            "attn_fwd_ex": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
             "attn_bwd_workspace_size": (sz, [i, i, i, i]),
             "attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
+            "attn_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz,
+                                vp]),
             "attn_bwd_preprocess": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
             "attn_bwd_main": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_dq_convert": (i, [vp, i, i, i, i, f, vp, sz, vp]),
@@ -126,10 +129,11 @@ def alloc_workspace(B: int, H: int, N: int, d: int, device) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None):
+def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None, window=0):
     """O = softmax(scale q k^T [+ causal mask]) v and the row log-sum-exp L.
 
     q, k, v: bf16 CUDA tensors [B, H, N, d] (d = 64 or 128), contiguous.
+    window > 0 (causal only): query i sees keys i - window < j <= i.
     Returns (O bf16 [B, H, N, d], L fp32 [B, H, N]).
     """
     B, H, N, d = _shape4(q, "q")
@@ -139,15 +143,15 @@ def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _check_tensor(out, "out", (B, H, N, d))
     _check_tensor(lse, "lse", (B, H, N), torch.float32)
-    st = load_library().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                 lse.data_ptr(), B, H, N, d, int(bool(causal)),
-                                 _default_scale(d, scale), _stream(stream))
-    _check("attn_fwd", st)
+    st = load_library().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), B, H, N, d, int(bool(causal)), int(window),
+                                    _default_scale(d, scale), _stream(stream))
+    _check("attn_fwd_ex", st)
     return out, lse
 
 
 def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, window=0):
     """dQ, dK, dV of exact attention (the fused backward, three kernels).
 
     o, lse: the forward's outputs; do: the upstream gradient of o.
@@ -164,12 +168,13 @@ def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv
         _check_tensor(t, n, (B, H, N, d))
     if workspace is None:
         workspace = alloc_workspace(B, H, N, d, q.device)
-    st = load_library().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                 do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                 dv.data_ptr(), B, H, N, d, int(bool(causal)),
-                                 _default_scale(d, scale), workspace.data_ptr(),
-                                 workspace.numel() * workspace.element_size(), _stream(stream))
-    _check("attn_bwd", st)
+    st = load_library().attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), B, H, N, d, int(bool(causal)), int(window),
+                                    _default_scale(d, scale), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check("attn_bwd_ex", st)
     return dq, dk, dv
 
 

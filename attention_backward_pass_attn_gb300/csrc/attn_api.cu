@@ -73,8 +73,17 @@ int make_shape(int B, int H, int N, int d, int causal, Shape* s, bool* empty) {
   s->causal = causal;
   s->n_tiles = int(n_tiles);
   s->Npad = int(n_tiles * 128);
+  s->window = 0;
   return ATTN_OK;
 }
+
+// The sliding window: only with the causal mask, and a window of N or more
+// keys is the causal mask itself.
+int check_window(int causal, int window) {
+  if (window < 0 || (window > 0 && !causal)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+void set_window(Shape* s, int window) { s->window = window >= s->N ? 0 : window; }
 
 bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
 
@@ -138,6 +147,32 @@ int make_acc_map(CUtensorMap* map, const float* acc, const Shape& s) {
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+// attn_bwd_main with a sliding window (0 = none).
+int bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
+             int B, int H, int N, int d, int causal, int window, float scale, void* workspace,
+             size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if ((st = check_window(causal, window)) != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  set_window(&s, window);
+  if ((st = check_ptrs({Q, K, V, dO, dK, dV})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  const Workspace ws = carve_workspace(workspace, s);
+  CUtensorMap mq, mk, mv, mdo, macc;
+  if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s) ||
+      make_tile_map(&mdo, dO, s) || make_acc_map(&macc, ws.acc, s))
+    return ATTN_ERR_CUDA;
+  return cuda_status(launch_bwd_main(mq, mk, mv, mdo, macc, dK, dV, ws, s, scale, err,
+                                     (cudaStream_t)stream));
+}
+
+
 }  // namespace attn
 
 using namespace attn;
@@ -169,12 +204,19 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
 
 int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N,
              int d, int causal, float scale, void* stream) {
+  return attn_fwd_ex(Q, K, V, O, L, B, H, N, d, causal, 0, scale, stream);
+}
+
+int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                int N, int d, int causal, int window, float scale, void* stream) {
   Shape s;
   bool empty = false;
   int st = make_shape(B, H, N, d, causal, &s, &empty);
   if (st != ATTN_OK) return st;
+  if ((st = check_window(causal, window)) != ATTN_OK) return st;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
   if (empty) return ATTN_OK;
+  set_window(&s, window);
   if ((st = check_ptrs({Q, K, V, O, L})) != ATTN_OK) return st;
   int* err = error_word_ptr();
   if (!err) return ATTN_ERR_CUDA;
@@ -200,23 +242,8 @@ int attn_bwd_preprocess(const void* O, const void* dO, const float* L, int B, in
 int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
                   int B, int H, int N, int d, int causal, float scale, void* workspace,
                   size_t workspace_bytes_, void* stream) {
-  Shape s;
-  bool empty = false;
-  int st = make_shape(B, H, N, d, causal, &s, &empty);
-  if (st != ATTN_OK) return st;
-  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
-  if (empty) return ATTN_OK;
-  if ((st = check_ptrs({Q, K, V, dO, dK, dV})) != ATTN_OK) return st;
-  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
-  int* err = error_word_ptr();
-  if (!err) return ATTN_ERR_CUDA;
-  const Workspace ws = carve_workspace(workspace, s);
-  CUtensorMap mq, mk, mv, mdo, macc;
-  if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s) ||
-      make_tile_map(&mdo, dO, s) || make_acc_map(&macc, ws.acc, s))
-    return ATTN_ERR_CUDA;
-  return cuda_status(launch_bwd_main(mq, mk, mv, mdo, macc, dK, dV, ws, s, scale, err,
-                                     (cudaStream_t)stream));
+  return bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, causal, 0, scale, workspace, workspace_bytes_,
+                  stream);
 }
 
 int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
@@ -236,18 +263,27 @@ int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const
 int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
              const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal,
              float scale, void* workspace, size_t workspace_bytes_, void* stream) {
+  return attn_bwd_ex(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, causal, 0, scale, workspace,
+                     workspace_bytes_, stream);
+}
+
+int attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                int causal, int window, float scale, void* workspace, size_t workspace_bytes_,
+                void* stream) {
   Shape s;
   bool empty = false;
   int st = make_shape(B, H, N, d, causal, &s, &empty);
   if (st != ATTN_OK) return st;
+  if ((st = check_window(causal, window)) != ATTN_OK) return st;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
   if (empty) return ATTN_OK;
   if ((st = check_ptrs({Q, K, V, O, dO, L, dQ, dK, dV})) != ATTN_OK) return st;
   if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
   st = attn_bwd_preprocess(O, dO, L, B, H, N, d, workspace, workspace_bytes_, stream);
   if (st != ATTN_OK) return st;
-  st = attn_bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, causal, scale, workspace, workspace_bytes_,
-                     stream);
+  st = bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, causal, window, scale, workspace,
+                workspace_bytes_, stream);
   if (st != ATTN_OK) return st;
   return attn_bwd_dq_convert(dQ, B, H, N, d, scale, workspace, workspace_bytes_, stream);
 }

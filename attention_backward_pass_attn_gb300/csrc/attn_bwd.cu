@@ -134,7 +134,7 @@ struct Layout {
 // within a block and 16 KB across blocks; an MN-major operand advances 2 KB
 // (16 rows) per k-step, its MN extent spanning blocks 16 KB apart (LBO).
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -143,7 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmAcc, const float* __restrict__ L2ws,
                          const float* __restrict__ Dws,
                          __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int BH,
-                         int N, int head_group, float scale, float scale_log2, int* err) {
+                         int N, int head_group, int window_arg, float scale, float scale_log2,
+                         int* err) {
+  // The sliding window has its own instantiation; without it the window code
+  // compiles away.
+  const int window = WINDOW ? window_arg : 0;
   using Ly = Layout<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -158,6 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Npad = n_tiles * 128;
   const int n_items = BH * n_tiles;
   const ItemMap imap{BH, n_tiles, head_group};
+  // Query tiles of the item with key/value tile jt: it0 .. it0 + n_it - 1.
+  // Under the causal mask they start at the diagonal; under a sliding window
+  // they end at the last query that still sees a key of the tile,
+  // jt * 128 + 127 + window - 1.
+  auto item_tiles = [&](int jt) {
+    int last = n_tiles - 1;
+    if (CAUSAL && window > 0) {
+      const int lq = (jt * 128 + 126 + window) >> 7;
+      if (lq < last) last = lq;
+    }
+    return last - (CAUSAL ? jt : 0) + 1;
+  };
   const int G = gridDim.x, b = blockIdx.x;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
@@ -222,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
       imap.decode(item, jt, bh);
-      const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
+      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt);
       const int next = snake_item(k + 1, b, G, n_items);
       int njt = 0, nbh = 0;
       if (next >= 0) imap.decode(next, njt, nbh);
@@ -323,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh_unused;
       imap.decode(item, jt, bh_unused);
-      const int n_it = n_tiles - (CAUSAL ? jt : 0);
+      const int n_it = item_tiles(jt);
       if (!(ok = mbar_wait_warp(bar(kBarKFull), k & 1, ctx, 0x220))) break;
       if (!(ok = mbar_wait_warp(bar(kBarQFull + (g & 1)), (g >> 1) & 1, ctx, 0x221))) break;
       tc_fence_after();
@@ -436,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
       imap.decode(item, jt, bh);
-      const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
+      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt);
       for (int it = 0; it < n_it; ++it, ++g) {
         const int s = g & 1, qt = it0 + it;
         if (!(ok = mbar_wait_warp(bar(kBarQFull + s), (g >> 1) & 1, ctx, 0x230))) break;
@@ -454,6 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
           tmem_wait_ld();
           const bool diag = CAUSAL && qt == jt;
+          // sliding window: query column q of this tile sees key row r only
+          // while (qt - jt) * 128 + q - r < window
+          const int dq_tile = (qt - jt) * 128;
+          const bool wedge = CAUSAL && window > 0 && dq_tile + 127 >= window;
           const float4* L2v4 = reinterpret_cast<const float4*>(L2v);
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
@@ -468,6 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (q0 + 1 < r) p1 = 0.f;
               if (q0 + 2 < r) p2 = 0.f;
               if (q0 + 3 < r) p3 = 0.f;
+            }
+            if (wedge) {
+              const int dq0 = dq_tile + 64 * h + 4 * c4 - r;
+              if (dq0 >= window) p0 = 0.f;
+              if (dq0 + 1 >= window) p1 = 0.f;
+              if (dq0 + 2 >= window) p2 = 0.f;
+              if (dq0 + 3 >= window) p3 = 0.f;
             }
             pk[2 * c4] = pack_bf16x2(p0, p1);
             pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
@@ -555,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
       imap.decode(item, jt, bh);
-      const int it0 = CAUSAL ? jt : 0, n_it = n_tiles - it0;
+      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt);
       for (int it = 0; it < n_it; ++it, ++g) {
         const int qt = it0 + it;
         // The four drain warps agree before any named barrier below, so that a
@@ -786,22 +813,23 @@ static int head_group(const Shape& s) {
   return int(hg);
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool WINDOW>
 static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                  const CUtensorMap& tmAcc, void* dK, void* dV,
                                  const Workspace& ws, const Shape& s, float scale, int* err,
                                  cudaStream_t stream) {
   using Ly = Layout<HD>;
-  auto kern = attn_bwd_main_kernel<HD, CAUSAL>;
-  cudaError_t e = set_smem_limit_once<attn_bwd_main_kernel<HD, CAUSAL>>(Ly::kBytes);
+  auto kern = attn_bwd_main_kernel<HD, CAUSAL, WINDOW>;
+  cudaError_t e = set_smem_limit_once<attn_bwd_main_kernel<HD, CAUSAL, WINDOW>>(Ly::kBytes);
   if (e != cudaSuccess) return e;
   // Persistent grid: at most one CTA per SM, each walking its work items.
   const long long n_items = (long long)s.n_tiles * s.BH;
   const dim3 grid(unsigned(n_items < num_sms() ? n_items : num_sms()));
   return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV, tmdO, tmAcc,
                        ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
-                       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, head_group(s), scale,
+                       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, head_group(s), s.window,
+                       scale,
                        scale * 1.4426950408889634f, err);
 }
 
@@ -831,15 +859,20 @@ cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO,
                             const CUtensorMap& tmAcc, void* dK, void* dV, const Workspace& ws,
                             const Shape& s, float scale, int* err, cudaStream_t stream) {
+  const bool w = s.causal && s.window > 0;
   if (s.d == 64)
-    return s.causal ? bwd::launch_main_t<64, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
-                                                   scale, err, stream)
-                    : bwd::launch_main_t<64, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
-                                                    scale, err, stream);
-  return s.causal ? bwd::launch_main_t<128, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
-                                                  scale, err, stream)
-                  : bwd::launch_main_t<128, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s,
-                                                   scale, err, stream);
+    return w ? bwd::launch_main_t<64, true, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s, scale,
+                                                  err, stream)
+           : s.causal ? bwd::launch_main_t<64, true, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws,
+                                                            s, scale, err, stream)
+                      : bwd::launch_main_t<64, false, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV,
+                                                             ws, s, scale, err, stream);
+  return w ? bwd::launch_main_t<128, true, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s, scale,
+                                                 err, stream)
+         : s.causal ? bwd::launch_main_t<128, true, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws,
+                                                           s, scale, err, stream)
+                    : bwd::launch_main_t<128, false, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV,
+                                                            ws, s, scale, err, stream);
 }
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,

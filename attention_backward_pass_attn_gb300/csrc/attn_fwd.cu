@@ -72,11 +72,15 @@ struct Layout {
 // within a block and 16 KB across blocks; an MN-major operand advances 2 KB
 // (16 rows) per k-step, its MN extent spanning blocks 16 KB apart (LBO).
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                    float* __restrict__ Lout, int BH, int N, float scale_log2, int* err) {
+                    float* __restrict__ Lout, int BH, int N, float scale_log2, int window_arg,
+                    int* err) {
+  // The sliding window has its own instantiation; without it the window code
+  // compiles away.
+  const int window = WINDOW ? window_arg : 0;
   using Ly = Layout<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -97,7 +101,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = CAUSAL ? (n_pairs - 1 - int(blockIdx.x / BH)) : int(blockIdx.x % n_pairs);
   const int qt_a = 2 * pair;
   const bool has_b = qt_a + 1 < n_tiles;
-  const int n_kv = CAUSAL ? min(n_tiles, qt_a + (has_b ? 2 : 1)) : n_tiles;
+  // Key/value tiles kv_lo .. kv_lo + n_kv - 1.  Under a sliding window the
+  // first query row of tile A sees keys from qt_a * 128 - window + 1 on;
+  // tiles wholly below that are skipped (tile B's extra leading tiles are
+  // masked for its rows).
+  const int kv_end = CAUSAL ? min(n_tiles, qt_a + (has_b ? 2 : 1)) : n_tiles;
+  const int lo_key = qt_a * 128 - window + 1;
+  const int kv_lo = (CAUSAL && window > 0 && lo_key > 0) ? lo_key / 128 : 0;
+  const int n_kv = kv_end - kv_lo;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
@@ -158,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kK + s * Ly::kTileBytes + cb * 16384, &tmK,
-                      bar(kBarKFull + s), cb * 64, j * 128, bh);
+                      bar(kBarKFull + s), cb * 64, (kv_lo + j) * 128, bh);
       }
       __syncwarp();
       if (j >= kStages && !mbar_wait_warp(bar(kBarVEmpty + s), (n - 1) & 1, ctx, 0x111)) break;
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < HD / 64; ++cb)
           tma_load_3d(sbase + Ly::kV + s * Ly::kTileBytes + cb * 16384, &tmV,
-                      bar(kBarVFull + s), cb * 64, j * 128, bh);
+                      bar(kBarVFull + s), cb * 64, (kv_lo + j) * 128, bh);
       }
       __syncwarp();
     }
@@ -270,12 +281,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
         tmem_wait_ld();
-        const int kv0 = j * 128;
-        if ((CAUSAL && kv0 + 127 > q_tile0) || kv0 + 128 > N) {
+        const int kv0 = (kv_lo + j) * 128;
+        // masked: above the diagonal, beyond N, or (sliding window) at least
+        // `window` keys behind the query
+        const bool below = CAUSAL && window > 0 && kv0 <= q_tile0 + 127 - window;
+        if ((CAUSAL && kv0 + 127 > q_tile0) || kv0 + 128 > N || below) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int kv = kv0 + c;
-            if ((CAUSAL && kv > q) || kv >= N) u[c] = __float_as_uint(-INFINITY);
+            if ((CAUSAL && kv > q) || kv >= N || (below && q - kv >= window))
+              u[c] = __float_as_uint(-INFINITY);
           }
         }
         float mx = __uint_as_float(u[0]);
@@ -365,19 +380,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD, bool CAUSAL>
+template <int HD, bool CAUSAL, bool WINDOW>
 static cudaError_t launch_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, void* O, float* L, const Shape& s,
                             float scale, int* err, cudaStream_t stream) {
   using Ly = Layout<HD>;
-  auto kern = attn_fwd_kernel<HD, CAUSAL>;
-  cudaError_t e = set_smem_limit_once<attn_fwd_kernel<HD, CAUSAL>>(Ly::kBytes);
+  auto kern = attn_fwd_kernel<HD, CAUSAL, WINDOW>;
+  cudaError_t e = set_smem_limit_once<attn_fwd_kernel<HD, CAUSAL, WINDOW>>(Ly::kBytes);
   if (e != cudaSuccess) return e;
   const int n_pairs = (s.n_tiles + 1) / 2;
   const dim3 grid(unsigned(n_pairs) * unsigned(s.BH));
   const float scale_log2 = scale * 1.4426950408889634f;
   return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV,
-                       reinterpret_cast<__nv_bfloat16*>(O), L, s.BH, s.N, scale_log2, err);
+                       reinterpret_cast<__nv_bfloat16*>(O), L, s.BH, s.N, scale_log2, s.window,
+                       err);
 }
 
 }  // namespace fwd
@@ -386,10 +402,14 @@ cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
                        void* O, float* L, const Shape& s, float scale, int* err,
                        cudaStream_t stream) {
   if (s.d == 64)
-    return s.causal ? fwd::launch_t<64, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
-                    : fwd::launch_t<64, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
-  return s.causal ? fwd::launch_t<128, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
-                  : fwd::launch_t<128, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+    return s.causal && s.window > 0
+               ? fwd::launch_t<64, true, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
+           : s.causal ? fwd::launch_t<64, true, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
+                      : fwd::launch_t<64, false, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+  return s.causal && s.window > 0
+             ? fwd::launch_t<128, true, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
+         : s.causal ? fwd::launch_t<128, true, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
+                    : fwd::launch_t<128, false, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
 }
 
 }  // namespace attn

@@ -20,6 +20,8 @@ struct Shape {
   int causal;
   int n_tiles;  // ceil(N / 128): 128-row tiles per head
   int Npad;     // n_tiles * 128
+  int window;   // causal sliding window: key j visible to query i iff i - window < j <= i;
+                // 0 = no window (also used for window >= N)
 };
 
 // Workspace carve-up (all fp32, 256-byte aligned sections):

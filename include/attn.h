@@ -71,6 +71,19 @@ int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int
              int N, int d, int causal, float scale, void* stream);
 
 /*
+ * Forward with a causal sliding window: key j is visible to query i when
+ * i - window < j <= i, so each query sees itself and the window - 1 keys
+ * before it (the banded causal mask of sliding-window attention, named in
+ * "Training - CUDA Moat Still Alive", section on attention variants, for
+ * Mistral 7B).  window = 0 means no window, and window >= N is the plain
+ * causal mask; otherwise as attn_fwd.  A window requires causal = 1 (else
+ * ATTN_ERR_INVALID_ARG, as for a negative window).  Key/value tiles wholly
+ * outside the band are skipped, so the cost grows with N * window, not N^2.
+ */
+int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                int N, int d, int causal, int window, float scale, void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this shape (0 for an empty
  * problem).  Holds, per head, D = rowsum(dO o O) and L scaled to base 2, each
  * [roundup(N,128)] fp32, and an fp32 dQ accumulator of roundup(N,128) x d.
@@ -90,6 +103,16 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
              const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
              int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward with a causal sliding window (see attn_fwd_ex); L must come from
+ * attn_fwd_ex with the same window.  Same workspace and steps as attn_bwd;
+ * window = 0 is attn_bwd.
+ */
+int attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                int causal, int window, float scale, void* workspace, size_t workspace_bytes,
+                void* stream);
 
 /*
  * Step 1 of attn_bwd: D_i = <dO_i, O_i> in fp32 and L_i * log2(e) into the

@@ -125,6 +125,24 @@ def test_bwd_validation(lib):
     assert lib.attn_watchdog_selftest(10, None) == ab.ATTN_ERR_INVALID_ARG
 
 
+def test_window_validation(lib):
+    """The sliding window is causal only and non-negative; checked before
+    anything else is looked at, empty problems included."""
+    def fwd_ex(causal, window, N=128, ptr=FAKE):
+        return lib.attn_fwd_ex(ptr, ptr, ptr, ptr, ptr, 1, 1, N, 64, causal, window, 0.125, None)
+
+    def bwd_ex(causal, window, N=128, ptr=FAKE):
+        need = lib.attn_bwd_workspace_size(1, 1, max(N, 0), 64)
+        return lib.attn_bwd_ex(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, N, 64, causal,
+                               window, 0.125, FAKE, need, None)
+    for f in (fwd_ex, bwd_ex):
+        assert f(0, 16) == ab.ATTN_ERR_INVALID_ARG
+        assert f(1, -1) == ab.ATTN_ERR_INVALID_ARG
+        assert f(0, 16, N=0, ptr=None) == ab.ATTN_ERR_INVALID_ARG
+        assert f(1, 16, N=0, ptr=None) == ab.ATTN_OK
+        assert f(1, 16, ptr=None) == ab.ATTN_ERR_INVALID_ARG  # null pointers still rejected
+
+
 def test_binding_checks_tensors():
     import torch
 
