@@ -32,6 +32,7 @@ class Workload:
     seed: int
     q_scale: float = 1.0   # Q is multiplied by this before the bf16 cast
     do_scale: float = 1.0  # dO is multiplied by this before the bf16 cast
+    window: int = 0        # causal sliding window (0 = none)
 
     @property
     def scale(self) -> float:
@@ -42,20 +43,28 @@ class Workload:
     def heads(self) -> int:
         return self.B * self.H
 
+    def pairs(self) -> float:
+        """Visible (query, key) pairs per head: N^2, N^2/2 under the causal
+        mask, and N*W - W^2/2 (the area of the band) under a window W < N."""
+        N, W = float(self.N), float(self.window)
+        if self.causal and 0 < W < N:
+            return N * W - W * W / 2
+        return N * N / 2 if self.causal else N * N
+
     def fwd_flops(self) -> float:
-        """4*B*H*N^2*d, halved under the causal mask."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
-        return f / 2 if self.causal else f
+        """4*d FLOPs per visible pair: 4*B*H*N^2*d, halved under the causal mask."""
+        return 4.0 * self.B * self.H * self.d * self.pairs()
 
     def bwd_flops(self) -> float:
-        """10*B*H*N^2*d (five N^2*d contractions), halved under the causal mask."""
-        f = 10.0 * self.B * self.H * self.N * self.N * self.d
-        return f / 2 if self.causal else f
+        """10*d FLOPs per visible pair (five contractions): 10*B*H*N^2*d, halved
+        under the causal mask."""
+        return 10.0 * self.B * self.H * self.d * self.pairs()
 
     def describe(self) -> str:
-        return ("B=%d H=%d N=%d d=%d %s q_scale=%g do_scale=%g seed=%d"
+        return ("B=%d H=%d N=%d d=%d %s%s q_scale=%g do_scale=%g seed=%d"
                 % (self.B, self.H, self.N, self.d,
                    "causal" if self.causal else "non-causal",
+                   " window=%d" % self.window if self.window else "",
                    self.q_scale, self.do_scale, self.seed))
 
     def with_shape(self, **kw) -> "Workload":
@@ -74,6 +83,13 @@ WORKLOADS = {
                                        seed=4),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
+
+# Sliding-window attention at the Mistral 7B window (4096 keys), measured
+# beside the workloads above.
+EXTRA_WORKLOADS = {
+    "b1h16n16384d128_w4096": Workload("b1h16n16384d128_w4096", 1, 16, 16384, 128, True,
+                                      seed=5, window=4096),
+}
 
 
 def make_inputs(w: Workload, dtype=torch.bfloat16):

@@ -22,7 +22,8 @@ Legs reported on the one JSON line (rank 0):
   roofline    the backward main kernel (tensor-bound) against the measured
               dense bf16 peak
   cpu_baseline the fp64 oracle on the host cores, on a bounded sample
-  d128_backward  the three d = 128 workloads (N >= 4096), main-kernel TF/s
+  d128_backward  the three d = 128 workloads (N >= 4096), main-kernel TF/s,
+              and sliding-window attention (N = 16384, a 4096-key window)
 
 --impl reference times the fp64 CPU oracle (the only reference this project
 has) on the same workload, metric and unit.
@@ -205,7 +206,7 @@ def time_workload(w, steps: int, warmup: int, flush, split=False):
     stream = torch.cuda.current_stream()
 
     def step():
-        ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream)
+        ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream, window=w.window)
         e[1].record(stream)
         if split:
             ab.attn_bwd_preprocess(o, do, lse, ws, stream=stream)
@@ -215,7 +216,7 @@ def time_workload(w, steps: int, warmup: int, flush, split=False):
             ab.attn_bwd_dq_convert(dq, ws, scale=w.scale, stream=stream)
         else:  # the public call: the same three kernels
             ab.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
-                        workspace=ws, stream=stream)
+                        workspace=ws, stream=stream, window=w.window)
 
     rec = []
     for i in range(warmup + steps):
@@ -346,7 +347,7 @@ def run_ours(args):
     else:
         torch.cuda.set_device(0)
     from attention_backward_pass_attn_gb300 import binding as ab
-    from attention_backward_pass_attn_gb300.inputs import WORKLOADS
+    from attention_backward_pass_attn_gb300.inputs import EXTRA_WORKLOADS, WORKLOADS
 
     ab.load_library()
     peaks, peak_src = load_peaks()
@@ -406,6 +407,19 @@ def run_ours(args):
                 "fwd_tflops": round(WORKLOADS[name].fwd_flops()
                                     / statistics.median(r["fwd"]) / 1e9, 1),
                 "main_ms_median": round(mm, 4),
+            }
+        # Sliding window (banded causal mask, 4096 keys): FLOPs are those of the
+        # visible band, N*W - W^2/2 pairs per head.
+        for name, sw in EXTRA_WORKLOADS.items():
+            rw = time_workload(sw, 10, 3, flush)
+            extra[name] = {
+                "window": sw.window,
+                "bwd_total_tflops": round(sw.bwd_flops() / statistics.median(rw["bwd"]) / 1e9, 1),
+                "bwd_total_frac": round(sw.bwd_flops() / statistics.median(rw["bwd"]) / 1e9
+                                        / peak_tf, 4),
+                "fwd_tflops": round(sw.fwd_flops() / statistics.median(rw["fwd"]) / 1e9, 1),
+                "bwd_ms_median": round(statistics.median(rw["bwd"]), 4),
+                "flops": "10*d*(N*W - W^2/2) per head (backward), 4*d*(...) (forward)",
             }
 
     if rank != 0:
