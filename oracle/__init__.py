@@ -68,15 +68,15 @@ def load(path: str | None = None):
         lib = ctypes.CDLL(lib_path)
         dp = ctypes.POINTER(ctypes.c_double)
         L = ctypes.c_long
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, L, L, L, ctypes.c_int, L,
+        lp = ctypes.POINTER(ctypes.c_long)
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, L, L, L, ctypes.c_int, L, lp,
                                         ctypes.c_double, dp, dp, ctypes.c_int]
         lib.oracle_attn_fwd.restype = ctypes.c_int
-        lib.oracle_attn_fwd_bwd.argtypes = [dp, dp, dp, dp, L, L, L, ctypes.c_int, L,
+        lib.oracle_attn_fwd_bwd.argtypes = [dp, dp, dp, dp, L, L, L, ctypes.c_int, L, lp,
                                             ctypes.c_double, dp, dp, dp, dp, dp,
                                             dp, ctypes.c_int]
         lib.oracle_attn_fwd_bwd.restype = ctypes.c_int
-        lp = ctypes.POINTER(ctypes.c_long)
-        lib.oracle_attn_head_rows.argtypes = [dp, dp, dp, dp, L, L, ctypes.c_int, L,
+        lib.oracle_attn_head_rows.argtypes = [dp, dp, dp, dp, L, L, ctypes.c_int, L, lp,
                                               ctypes.c_double, L, lp, L, lp, dp, dp, dp,
                                               dp, dp, ctypes.c_int]
         lib.oracle_attn_head_rows.restype = ctypes.c_int
@@ -101,23 +101,43 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
+def _doc_map(doc, heads_per_batch: int, rows: int):
+    """A document map [B, N] (first position of each position's document),
+    repeated for every head: [B*H, N] C longs, or None."""
+    if doc is None:
+        return None, None
+    if hasattr(doc, "detach"):
+        doc = doc.detach().to("cpu").numpy()
+    a = np.asarray(doc, dtype=np.int64)
+    if a.ndim == 1:
+        a = a[None, :]
+    if a.shape[-1] != rows:
+        raise ValueError("document map must have N = %d columns" % rows)
+    a = np.ascontiguousarray(np.repeat(a, heads_per_batch, axis=0).astype(np.dtype("l")))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+
+
 def max_threads(lib=None) -> int:
     return int((lib or load()).oracle_max_threads())
 
 
 def attention_forward(q, k, v, causal: bool, scale: float, threads: int = 0, lib=None,
-                      window: int = 0):
+                      window: int = 0, doc=None):
     """O [B,H,N,d] and L [B,H,N] (natural-log log-sum-exp), both float64.
 
-    window > 0 (causal only): query i sees keys i - window < j <= i."""
+    window > 0 (causal only): query i sees keys i - window < j <= i.
+    doc [B, N] (causal only): query i sees keys from doc[b, i] on, the first
+    position of its document."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     if q.ndim != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must share the shape [B, H, N, d]")
     B, H, N, d = q.shape
     o = np.zeros_like(q)
     lse = np.zeros((B, H, N), dtype=np.float64)
+    doc_a, doc_p = _doc_map(doc, H, N)
     st = (lib or load()).oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B * H, N, d,
-                                         int(bool(causal)), int(window), float(scale), _ptr(o),
+                                         int(bool(causal)), int(window), doc_p, float(scale),
+                                         _ptr(o),
                                          _ptr(lse), int(threads))
     if st != 0:
         raise RuntimeError("oracle_attn_fwd failed with status %d" % st)
@@ -125,7 +145,7 @@ def attention_forward(q, k, v, causal: bool, scale: float, threads: int = 0, lib
 
 
 def attention_forward_backward(q, k, v, do, causal: bool, scale: float,
-                               threads: int = 0, lib=None, window: int = 0) -> dict:
+                               threads: int = 0, lib=None, window: int = 0, doc=None) -> dict:
     """Exact forward and analytic backward in float64.
 
     Returns a dict with O, L, D (= rowsum(dO * O)), dQ, dK, dV.
@@ -137,9 +157,10 @@ def attention_forward_backward(q, k, v, do, causal: bool, scale: float,
     out = {name: np.zeros_like(q) for name in ("O", "dQ", "dK", "dV")}
     out["L"] = np.zeros((B, H, N), dtype=np.float64)
     out["D"] = np.zeros((B, H, N), dtype=np.float64)
+    doc_a, doc_p = _doc_map(doc, H, N)
     st = (lib or load()).oracle_attn_fwd_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, N, d, int(bool(causal)), int(window),
-        float(scale), _ptr(out["O"]), _ptr(out["L"]), _ptr(out["D"]),
+        doc_p, float(scale), _ptr(out["O"]), _ptr(out["L"]), _ptr(out["D"]),
         _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), int(threads))
     if st != 0:
         raise RuntimeError("oracle_attn_fwd_bwd failed with status %d" % st)
@@ -147,7 +168,7 @@ def attention_forward_backward(q, k, v, do, causal: bool, scale: float,
 
 
 def attention_head_rows(q, k, v, do, causal: bool, scale: float, q_rows, k_rows,
-                        threads: int = 0, lib=None, window: int = 0) -> dict:
+                        threads: int = 0, lib=None, window: int = 0, doc=None) -> dict:
     """Sampled rows of one head ([N, d] inputs), for shapes too large to do in full.
 
     Returns O, L, dQ at the query rows ``q_rows`` and dK, dV at the key rows
@@ -163,8 +184,9 @@ def attention_head_rows(q, k, v, do, causal: bool, scale: float, q_rows, k_rows,
     out = {"O": np.zeros((len(qr), d)), "L": np.zeros(len(qr)), "dQ": np.zeros((len(qr), d)),
            "dK": np.zeros((len(kr), d)), "dV": np.zeros((len(kr), d))}
     lp = ctypes.POINTER(ctypes.c_long)
+    doc_a, doc_p = _doc_map(doc, 1, N)  # one head: doc is [N]
     st = (lib or load()).oracle_attn_head_rows(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, d, int(bool(causal)), int(window),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(do), N, d, int(bool(causal)), int(window), doc_p,
         float(scale),
         len(qr), qr.ctypes.data_as(lp), len(kr), kr.ctypes.data_as(lp), _ptr(out["O"]),
         _ptr(out["L"]), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), int(threads))

@@ -39,6 +39,12 @@
  * CUDA Moat Still Alive", section on attention variants, as the Mistral 7B
  * mask).  M_ij = -inf outside the band; W >= N is the plain causal mask.
  *
+ * Documents.  With causal and a document map (several sequences packed into
+ * one), key j is visible to query i only when both belong to the same
+ * document: doc[i] <= j <= i, where doc[i] is the first position of the
+ * document holding position i (FlexAttention's document mask, named in the
+ * same section).  A window and documents combine: j >= max(doc[i], i - W + 1).
+ *
  * How.  Three passes over the rows of each head, each a direct evaluation of
  * the definition above, all in double precision:
  *   pass 1, over query rows i:   L_i, O_i, D_i
@@ -71,22 +77,33 @@ static double dot(const double *a, const double *b, long d) {
   return acc;
 }
 
+/* The mask of one head: causal or not, a sliding window (0 = none), and the
+ * document map of the head ([N], NULL = one document). */
+typedef struct {
+  int causal;
+  long window;
+  const long *doc;
+} Mask;
+
 /* One past the last key row i may attend to. */
 static long row_len(long i, long N, int causal) { return causal ? i + 1 : N; }
 
-/* The first key row i may attend to: under a sliding window W, i - W + 1. */
-static long row_start(long i, int causal, long window) {
-  return (causal && window > 0 && i - window + 1 > 0) ? i - window + 1 : 0;
+/* The first key row i may attend to: under a sliding window W, i - W + 1;
+ * with documents, no earlier than the start of i's document. */
+static long row_start(long i, const Mask *mk) {
+  long window = mk->window;
+  long lo = (mk->causal && window > 0 && i - window + 1 > 0) ? i - window + 1 : 0;
+  if (mk->causal && mk->doc && mk->doc[i] > lo) lo = mk->doc[i];
+  return lo;
 }
 
 /* Fill srow[j] = scale * <q_i, k_j> for the unmasked keys j of row i, which
  * are lo <= j < n; set *lo and return n. */
 static long scores_row(const double *Qh, const double *Kh, long i, long N,
-                       long d, int causal, long window, double scale, double *srow,
-                       long *lo) {
-  long n = row_len(i, N, causal);
+                       long d, const Mask *mk, double scale, double *srow, long *lo) {
+  long n = row_len(i, N, mk->causal);
   const double *qi = Qh + i * d;
-  *lo = row_start(i, causal, window);
+  *lo = row_start(i, mk);
   for (long j = *lo; j < n; ++j) srow[j] = scale * dot(qi, Kh + j * d, d);
   return n;
 }
@@ -102,11 +119,11 @@ static void set_threads(int nthreads) {
 /* L_i, O_i and (when dOh is given) D_i = <dO_i, O_i> for one query row i of
  * one head. */
 static void fwd_row(const double *Qh, const double *Kh, const double *Vh,
-                    const double *dOh, long N, long d, int causal, long window,
+                    const double *dOh, long N, long d, const Mask *mk,
                     double scale, long i, double *srow, double *Li_out, double *Oi,
                     double *Di_out) {
   long lo;
-  long n = scores_row(Qh, Kh, i, N, d, causal, window, scale, srow, &lo);
+  long n = scores_row(Qh, Kh, i, N, d, mk, scale, srow, &lo);
   double m = -INFINITY;
   for (long j = lo; j < n; ++j) m = srow[j] > m ? srow[j] : m;
   double l = 0.0;
@@ -125,7 +142,8 @@ static void fwd_row(const double *Qh, const double *Kh, const double *Vh,
 /* Pass 1: L, O and D for every query row. */
 static int pass_forward(const double *Q, const double *K, const double *V,
                         const double *dO, long BH, long N, long d, int causal,
-                        long window, double scale, double *O, double *L, double *D) {
+                        long window, const long *doc, double scale, double *O, double *L,
+                        double *D) {
   int failed = 0;
 #pragma omp parallel
   {
@@ -138,8 +156,9 @@ static int pass_forward(const double *Q, const double *K, const double *V,
     for (long h = 0; h < BH; ++h) {
       for (long i = 0; i < N; ++i) {
         if (!srow) continue;
+        const Mask mk = {causal, window, doc ? doc + h * N : NULL};
         fwd_row(Q + h * N * d, K + h * N * d, V + h * N * d,
-                dO ? dO + h * N * d : NULL, N, d, causal, window, scale, i, srow,
+                dO ? dO + h * N * d : NULL, N, d, &mk, scale, i, srow,
                 L + h * N + i, O + (h * N + i) * d, D ? D + h * N + i : NULL);
       }
     }
@@ -151,11 +170,10 @@ static int pass_forward(const double *Q, const double *K, const double *V,
 /* dQ_i = s * sum_j P_ij (dP_ij - D_i) k_j for one query row i of one head. */
 static void dq_row(const double *Qh, const double *Kh, const double *Vh,
                    const double *dOh, double Li, double Di, long N, long d,
-                   int causal, long window, double scale, long i, double *srow,
-                   double *dQi) {
+                   const Mask *mk, double scale, long i, double *srow, double *dQi) {
   const double *dOi = dOh + i * d;
   long lo;
-  long n = scores_row(Qh, Kh, i, N, d, causal, window, scale, srow, &lo);
+  long n = scores_row(Qh, Kh, i, N, d, mk, scale, srow, &lo);
   for (long c = 0; c < d; ++c) dQi[c] = 0.0;
   for (long j = lo; j < n; ++j) {
     double p = exp(srow[j] - Li);
@@ -169,16 +187,20 @@ static void dq_row(const double *Qh, const double *Kh, const double *Vh,
 
 /* dK_j = s * sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i for one key row j of
  * one head.  Under the causal mask, key j is seen by query rows i >= j only;
- * under a sliding window W also only by rows i < j + W. */
+ * under a sliding window W also only by rows i < j + W; with documents only
+ * by rows of its own document. */
 static void dkdv_row(const double *Qh, const double *Kh, const double *Vh,
                      const double *dOh, const double *Lh, const double *Dh, long N,
-                     long d, int causal, long window, double scale, long j,
-                     double *dKj, double *dVj) {
+                     long d, const Mask *mk, double scale, long j, double *dKj,
+                     double *dVj) {
   const double *kj = Kh + j * d, *vj = Vh + j * d;
+  const int causal = mk->causal;
+  const long window = mk->window;
   for (long c = 0; c < d; ++c) dKj[c] = dVj[c] = 0.0;
   long i0 = causal ? j : 0;
   long i1 = (causal && window > 0 && j + window < N) ? j + window : N;
   for (long i = i0; i < i1; ++i) {
+    if (row_start(i, mk) > j) continue;  /* j is outside row i's document */
     const double *qi = Qh + i * d, *dOi = dOh + i * d;
     double sij = scale * dot(qi, kj, d);
     double p = exp(sij - Lh[i]);
@@ -195,7 +217,8 @@ static void dkdv_row(const double *Qh, const double *Kh, const double *Vh,
 /* Pass 2: dQ for every query row. */
 static int pass_dq(const double *Q, const double *K, const double *V,
                    const double *dO, const double *L, const double *D, long BH,
-                   long N, long d, int causal, long window, double scale, double *dQ) {
+                   long N, long d, int causal, long window, const long *doc, double scale,
+                   double *dQ) {
   int failed = 0;
 #pragma omp parallel
   {
@@ -208,8 +231,9 @@ static int pass_dq(const double *Q, const double *K, const double *V,
     for (long h = 0; h < BH; ++h) {
       for (long i = 0; i < N; ++i) {
         if (!srow) continue;
+        const Mask mk = {causal, window, doc ? doc + h * N : NULL};
         dq_row(Q + h * N * d, K + h * N * d, V + h * N * d, dO + h * N * d,
-               L[h * N + i], D[h * N + i], N, d, causal, window, scale, i, srow,
+               L[h * N + i], D[h * N + i], N, d, &mk, scale, i, srow,
                dQ + (h * N + i) * d);
       }
     }
@@ -221,13 +245,14 @@ static int pass_dq(const double *Q, const double *K, const double *V,
 /* Pass 3: dK and dV for every key row. */
 static int pass_dkdv(const double *Q, const double *K, const double *V,
                      const double *dO, const double *L, const double *D,
-                     long BH, long N, long d, int causal, long window, double scale,
-                     double *dK, double *dV) {
+                     long BH, long N, long d, int causal, long window, const long *doc,
+                     double scale, double *dK, double *dV) {
 #pragma omp parallel for collapse(2) schedule(dynamic, 16)
   for (long h = 0; h < BH; ++h) {
     for (long j = 0; j < N; ++j) {
+      const Mask mk = {causal, window, doc ? doc + h * N : NULL};
       dkdv_row(Q + h * N * d, K + h * N * d, V + h * N * d, dO + h * N * d,
-               L + h * N, D + h * N, N, d, causal, window, scale, j,
+               L + h * N, D + h * N, N, d, &mk, scale, j,
                dK + (h * N + j) * d, dV + (h * N + j) * d);
     }
   }
@@ -235,9 +260,17 @@ static int pass_dkdv(const double *Q, const double *K, const double *V,
 }
 
 static int check_args(const void *a, const void *b, const void *c, long BH,
-                      long N, long d, int causal, long window, double scale) {
+                      long N, long d, int causal, long window, const long *doc,
+                      double scale) {
   if (BH < 0 || N < 0 || d < 0) return ORACLE_ERR_ARG;
   if (window < 0 || (window > 0 && !causal)) return ORACLE_ERR_ARG; /* the band is causal */
+  if (doc && !causal) return ORACLE_ERR_ARG;                         /* so are documents */
+  /* a document map: doc[i] = i (a document starts) or doc[i - 1] */
+  for (long h = 0; doc && h < BH; ++h)
+    for (long i = 0; i < N; ++i) {
+      long v = doc[h * N + i];
+      if (!(v == i || (i > 0 && v == doc[h * N + i - 1]))) return ORACLE_ERR_ARG;
+    }
   if (BH * N * d > 0 && (!a || !b || !c)) return ORACLE_ERR_ARG;
   if (!(scale == scale)) return ORACLE_ERR_ARG; /* NaN */
   return ORACLE_OK;
@@ -245,31 +278,31 @@ static int check_args(const void *a, const void *b, const void *c, long BH,
 
 /* Forward only: O [BH][N][d] and L [BH][N]. */
 int oracle_attn_fwd(const double *Q, const double *K, const double *V, long BH,
-                    long N, long d, int causal, long window, double scale, double *O,
-                    double *L, int nthreads) {
-  int st = check_args(Q, K, V, BH, N, d, causal, window, scale);
+                    long N, long d, int causal, long window, const long *doc,
+                    double scale, double *O, double *L, int nthreads) {
+  int st = check_args(Q, K, V, BH, N, d, causal, window, doc, scale);
   if (st) return st;
   if (BH * N == 0) return ORACLE_OK;
   if (!O || !L) return ORACLE_ERR_ARG;
   set_threads(nthreads);
-  return pass_forward(Q, K, V, NULL, BH, N, d, causal, window, scale, O, L, NULL);
+  return pass_forward(Q, K, V, NULL, BH, N, d, causal, window, doc, scale, O, L, NULL);
 }
 
 /* Forward and backward: O, L, D = rowsum(dO * O), dQ, dK, dV. */
 int oracle_attn_fwd_bwd(const double *Q, const double *K, const double *V,
                         const double *dO, long BH, long N, long d, int causal,
-                        long window, double scale, double *O, double *L, double *D,
-                        double *dQ, double *dK, double *dV, int nthreads) {
-  int st = check_args(Q, K, V, BH, N, d, causal, window, scale);
+                        long window, const long *doc, double scale, double *O, double *L,
+                        double *D, double *dQ, double *dK, double *dV, int nthreads) {
+  int st = check_args(Q, K, V, BH, N, d, causal, window, doc, scale);
   if (st) return st;
   if (BH * N == 0) return ORACLE_OK;
   if (!dO || !O || !L || !D || !dQ || !dK || !dV) return ORACLE_ERR_ARG;
   set_threads(nthreads);
-  st = pass_forward(Q, K, V, dO, BH, N, d, causal, window, scale, O, L, D);
+  st = pass_forward(Q, K, V, dO, BH, N, d, causal, window, doc, scale, O, L, D);
   if (st) return st;
-  st = pass_dq(Q, K, V, dO, L, D, BH, N, d, causal, window, scale, dQ);
+  st = pass_dq(Q, K, V, dO, L, D, BH, N, d, causal, window, doc, scale, dQ);
   if (st) return st;
-  return pass_dkdv(Q, K, V, dO, L, D, BH, N, d, causal, window, scale, dK, dV);
+  return pass_dkdv(Q, K, V, dO, L, D, BH, N, d, causal, window, doc, scale, dK, dV);
 }
 
 /* Threads the oracle would use (1 without OpenMP). */
@@ -288,11 +321,11 @@ int oracle_max_threads(void) {
  * dK_rows, dV_rows [nk][d].  Q, K, V, dO are one head, [N][d]. */
 int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
                           const double *dO, long N, long d, int causal, long window,
-                          double scale, long nq, const long *qrows, long nk,
+                          const long *doc, double scale, long nq, const long *qrows, long nk,
                           const long *krows, double *O_rows, double *L_rows,
                           double *dQ_rows, double *dK_rows, double *dV_rows,
                           int nthreads) {
-  int st = check_args(Q, K, V, 1, N, d, causal, window, scale);
+  int st = check_args(Q, K, V, 1, N, d, causal, window, doc, scale);
   if (st) return st;
   if (nq < 0 || nk < 0 || (nq && (!qrows || !O_rows || !L_rows || !dQ_rows)) ||
       (nk && (!krows || !dK_rows || !dV_rows)) || !dO)
@@ -303,6 +336,7 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
     if (krows[t] < 0 || krows[t] >= N) return ORACLE_ERR_ARG;
   if (N == 0) return ORACLE_OK;
   set_threads(nthreads);
+  const Mask mk = {causal, window, doc};
   if (nk == 0) {
     /* Query rows only: O_i, L_i, D_i and dQ_i depend on row i alone. */
     int failed = 0;
@@ -318,10 +352,9 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
       for (long t = 0; t < nq; ++t) {
         if (!srow) continue;
         long i = qrows[t];
-        fwd_row(Q, K, V, dO, N, d, causal, window, scale, i, srow, &Li, O_rows + t * d,
-                &Di);
+        fwd_row(Q, K, V, dO, N, d, &mk, scale, i, srow, &Li, O_rows + t * d, &Di);
         L_rows[t] = Li;
-        dq_row(Q, K, V, dO, Li, Di, N, d, causal, window, scale, i, srow, dQ_rows + t * d);
+        dq_row(Q, K, V, dO, Li, Di, N, d, &mk, scale, i, srow, dQ_rows + t * d);
       }
       free(srow);
     }
@@ -334,7 +367,7 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
     free(O); free(L); free(D);
     return ORACLE_ERR_NOMEM;
   }
-  st = pass_forward(Q, K, V, dO, 1, N, d, causal, window, scale, O, L, D);
+  st = pass_forward(Q, K, V, dO, 1, N, d, causal, window, doc, scale, O, L, D);
   if (!st) {
     int failed = 0;
 #pragma omp parallel
@@ -350,13 +383,12 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
         long i = qrows[t];
         memcpy(O_rows + t * d, O + i * d, sizeof(double) * (size_t)d);
         L_rows[t] = L[i];
-        dq_row(Q, K, V, dO, L[i], D[i], N, d, causal, window, scale, i, srow,
-               dQ_rows + t * d);
+        dq_row(Q, K, V, dO, L[i], D[i], N, d, &mk, scale, i, srow, dQ_rows + t * d);
       }
 #pragma omp for schedule(dynamic, 1)
       for (long t = 0; t < nk; ++t)
-        dkdv_row(Q, K, V, dO, L, D, N, d, causal, window, scale, krows[t],
-                 dK_rows + t * d, dV_rows + t * d);
+        dkdv_row(Q, K, V, dO, L, D, N, d, &mk, scale, krows[t], dK_rows + t * d,
+                 dV_rows + t * d);
       free(srow);
     }
     if (failed) st = ORACLE_ERR_NOMEM;

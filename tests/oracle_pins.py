@@ -18,6 +18,11 @@ i - W < j <= i -- has pins of its own: finite differences, the closed forms
 W = 1 and W >= N, truncation to the window's keys, the brute force with the
 band, and PyTorch with an explicit band mask.
 
+Document masks (several sequences packed into one; a query sees keys of its
+own document only, causally) are pinned by equality with separate causal
+attention over each document, a single document being plain causal (bit for
+bit), the brute force, and PyTorch with an explicit block-diagonal mask.
+
 The method is exact attention as named by "Training Transformers and Hybrid
 models on AMD Instinct MI300X Accelerators", section "Flash Attention"; the
 pages print no worked example, so every pin is mathematical.
@@ -36,9 +41,20 @@ def _rand(rng, shape, std=1.0):
     return rng.standard_normal(shape) * std
 
 
-def _fb(lib, q, k, v, do, causal, scale, window=0):
+def _fb(lib, q, k, v, do, causal, scale, window=0, doc=None):
     return oracle.attention_forward_backward(q, k, v, do, causal, scale, lib=lib,
-                                             window=window)
+                                             window=window, doc=doc)
+
+
+def doc_map(lengths):
+    """Document map of documents of the given lengths, packed in order:
+    position i maps to the first position of its document."""
+    out = []
+    start = 0
+    for n in lengths:
+        out.extend([start] * n)
+        start += n
+    return np.array(out, dtype=np.int64)
 
 
 def _close(a, b, rtol, atol=0.0, what=""):
@@ -225,13 +241,14 @@ def pin_permutation(lib):
 # --------------------------------------------------------------------------
 # Brute force over the full matrices, pure Python loops, tiny N.
 # --------------------------------------------------------------------------
-def _brute(q, k, v, do, causal, s, window=0):
+def _brute(q, k, v, do, causal, s, window=0, doc=None):
     N, d = len(q), len(q[0])
 
     def visible(i, j):
         if not causal:
             return True
-        return j <= i and (window == 0 or i - j < window)
+        same_doc = doc is None or doc[i] == doc[j]
+        return j <= i and (window == 0 or i - j < window) and same_doc
 
     S = [[(s * sum(q[i][c] * k[j][c] for c in range(d)) if visible(i, j)
            else -math.inf) for j in range(N)] for i in range(N)]
@@ -426,6 +443,81 @@ def pin_window_torch_fp64(lib):
         _close(out["dV"], tv.grad.numpy(), 1e-10, what="window torch dV")
 
 
+# --------------------------------------------------------------------------
+# Document masks (packed sequences).
+# --------------------------------------------------------------------------
+def pin_doc_separate_sequences(lib):
+    """Packed documents give exactly what each document gives on its own under
+    the plain causal mask: O, L, D, dQ, dK, dV, row by row."""
+    rng = np.random.default_rng(26)
+    for lengths in ((5, 1, 9, 3), (17,), (1, 1, 1), (12, 30, 7)):
+        N, d, s = sum(lengths), 4, 0.6
+        q, k, v, do = (_rand(rng, (2, 2, N, d)) for _ in range(4))
+        dm = np.stack([doc_map(lengths), doc_map(lengths)])
+        packed = _fb(lib, q, k, v, do, True, s, doc=dm)
+        start = 0
+        for n in lengths:
+            sl = slice(start, start + n)
+            alone = _fb(lib, q[:, :, sl], k[:, :, sl], v[:, :, sl], do[:, :, sl], True, s)
+            for name in ("O", "dQ", "dK", "dV"):
+                _close(packed[name][:, :, sl], alone[name], 1e-13,
+                       what="doc %s lengths=%s" % (name, lengths))
+            for name in ("L", "D"):
+                _close(packed[name][:, :, sl], alone[name], 1e-13, what="doc %s" % name)
+            start += n
+
+
+def pin_doc_single_document_is_causal(lib):
+    rng = np.random.default_rng(27)
+    N, d, s = 33, 3, 0.7
+    q, k, v, do = (_rand(rng, (1, 2, N, d)) for _ in range(4))
+    one = _fb(lib, q, k, v, do, True, s, doc=np.zeros((1, N), dtype=np.int64))
+    causal = _fb(lib, q, k, v, do, True, s)
+    for name in causal:
+        assert np.array_equal(one[name], causal[name]), name
+
+
+def pin_doc_brute_force(lib):
+    rng = np.random.default_rng(28)
+    for lengths, W in (((3, 5), 0), ((2, 2, 4), 0), ((6, 2), 3), ((1, 7), 2)):
+        N, d, s = sum(lengths), 3, 0.8
+        q, k, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(4))
+        dm = doc_map(lengths)
+        out = _fb(lib, q, k, v, do, True, s, window=W, doc=dm[None])
+        ref = _brute(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(),
+                     do[0, 0].tolist(), True, s, window=W, doc=dm.tolist())
+        for name in ("O", "dQ", "dK", "dV", "L", "D"):
+            _close(out[name][0, 0], np.array(ref[name]), 1e-12,
+                   what="doc brute %s lengths=%s W=%d" % (name, lengths, W))
+
+
+def pin_doc_torch_fp64(lib):
+    import torch
+
+    rng = np.random.default_rng(29)
+    for lengths, W in (((40, 24), 0), ((100, 1, 30), 0), ((70, 90, 140), 50)):
+        N, d = sum(lengths), 16
+        q, k, v, do = (_rand(rng, (1, 2, N, d)) for _ in range(4))
+        s = 1.0 / math.sqrt(d)
+        dm = doc_map(lengths)
+        out = _fb(lib, q, k, v, do, True, s, window=W, doc=dm[None])
+        i = torch.arange(N).view(N, 1)
+        j = torch.arange(N).view(1, N)
+        dt = torch.tensor(dm)
+        allowed = (j <= i) & (dt.view(N, 1) == dt.view(1, N))
+        if W:
+            allowed &= i - j < W
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True)
+                      for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=allowed,
+                                                              scale=s)
+        to.backward(torch.tensor(do, dtype=torch.float64))
+        _close(out["O"], to.detach().numpy(), 1e-11, what="doc torch O")
+        _close(out["dQ"], tq.grad.numpy(), 1e-10, what="doc torch dQ")
+        _close(out["dK"], tk.grad.numpy(), 1e-10, what="doc torch dK")
+        _close(out["dV"], tv.grad.numpy(), 1e-10, what="doc torch dV")
+
+
 ALL_PINS = [
     pin_finite_differences,
     pin_single_key,
@@ -442,4 +534,8 @@ ALL_PINS = [
     pin_window_truncation,
     pin_window_brute_force,
     pin_window_torch_fp64,
+    pin_doc_separate_sequences,
+    pin_doc_single_document_is_causal,
+    pin_doc_brute_force,
+    pin_doc_torch_fp64,
 ]

@@ -26,8 +26,9 @@ MUTANTS = {
     "causal_excludes_diagonal": ("return causal ? i + 1 : N;", "return causal ? (i > 0 ? i : 1) : N;"),
     "dk_uses_k_not_q": ("dKj[c] += ds * qi[c];", "dKj[c] += ds * kj[c];"),
     "window_one_key_too_many": ("? i - window + 1 : 0;", "? i - window : 0;"),
-    "dkdv_ignores_window": ("long i1 = (causal && window > 0 && j + window < N) ? j + window : N;",
-                            "long i1 = N;"),
+    "doc_start_one_early": ("if (mk->causal && mk->doc && mk->doc[i] > lo) lo = mk->doc[i];",
+                            "if (mk->causal && mk->doc && mk->doc[i] - 1 > lo) lo = mk->doc[i] - 1;"),
+    "dkdv_ignores_documents": ("if (row_start(i, mk) > j) continue;", ""),
     "D_uses_wrong_row": ("if (dOh && Di_out) *Di_out = dot(dOh + i * d, Oi, d);",
                          "if (dOh && Di_out) *Di_out = dot(dOh + (N - 1 - i) * d, Oi, d);"),
 }
