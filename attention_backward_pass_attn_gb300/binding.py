@@ -54,11 +54,11 @@ def load_library(path: str | None = None):
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         sig = {
             "attn_fwd": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]),
-            "attn_fwd_ex": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
+            "attn_fwd_ex": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp]),
             "attn_bwd_workspace_size": (sz, [i, i, i, i]),
             "attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
-            "attn_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz,
-                                vp]),
+            "attn_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp,
+                                sz, vp]),
             "attn_bwd_preprocess": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
             "attn_bwd_main": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_dq_convert": (i, [vp, i, i, i, i, f, vp, sz, vp]),
@@ -114,6 +114,14 @@ def _check_tensor(t: torch.Tensor, name: str, shape, dtype=torch.bfloat16):
         raise ValueError("%s must be contiguous" % name)
 
 
+def _doc_ptr(doc, B: int, N: int):
+    """Device pointer of a document map (int32 CUDA tensor [B, N], contiguous), or None."""
+    if doc is None:
+        return None
+    _check_tensor(doc, "doc", (B, N), torch.int32)
+    return doc.data_ptr()
+
+
 def _default_scale(d: int, scale):
     return 1.0 / math.sqrt(d) if scale is None else float(scale)
 
@@ -129,11 +137,14 @@ def alloc_workspace(B: int, H: int, N: int, d: int, device) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None, window=0):
+def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None, window=0,
+             doc=None):
     """O = softmax(scale q k^T [+ causal mask]) v and the row log-sum-exp L.
 
     q, k, v: bf16 CUDA tensors [B, H, N, d] (d = 64 or 128), contiguous.
     window > 0 (causal only): query i sees keys i - window < j <= i.
+    doc (causal only): int32 CUDA tensor [B, N], the first position of each
+    position's document; query i sees keys doc[b, i] <= j <= i.
     Returns (O bf16 [B, H, N, d], L fp32 [B, H, N]).
     """
     B, H, N, d = _shape4(q, "q")
@@ -145,13 +156,14 @@ def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None,
     _check_tensor(lse, "lse", (B, H, N), torch.float32)
     st = load_library().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                     lse.data_ptr(), B, H, N, d, int(bool(causal)), int(window),
-                                    _default_scale(d, scale), _stream(stream))
+                                    _doc_ptr(doc, B, N), _default_scale(d, scale),
+                                    _stream(stream))
     _check("attn_fwd_ex", st)
     return out, lse
 
 
 def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None, window=0):
+             workspace=None, stream=None, window=0, doc=None):
     """dQ, dK, dV of exact attention (the fused backward, three kernels).
 
     o, lse: the forward's outputs; do: the upstream gradient of o.
@@ -171,7 +183,8 @@ def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv
     st = load_library().attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                     do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                     dv.data_ptr(), B, H, N, d, int(bool(causal)), int(window),
-                                    _default_scale(d, scale), workspace.data_ptr(),
+                                    _doc_ptr(doc, B, N), _default_scale(d, scale),
+                                    workspace.data_ptr(),
                                     workspace.numel() * workspace.element_size(),
                                     _stream(stream))
     _check("attn_bwd_ex", st)

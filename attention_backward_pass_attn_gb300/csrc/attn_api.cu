@@ -74,16 +74,24 @@ int make_shape(int B, int H, int N, int d, int causal, Shape* s, bool* empty) {
   s->n_tiles = int(n_tiles);
   s->Npad = int(n_tiles * 128);
   s->window = 0;
+  s->H = H;
+  s->doc = nullptr;
   return ATTN_OK;
 }
 
-// The sliding window: only with the causal mask, and a window of N or more
-// keys is the causal mask itself.
-int check_window(int causal, int window) {
+// The sliding window and the document map: only with the causal mask; a
+// window of N or more keys is the causal mask itself.  The map is read by
+// the kernels as int32 and must be 4-byte aligned.
+int check_mask(int causal, int window, const int* doc) {
   if (window < 0 || (window > 0 && !causal)) return ATTN_ERR_INVALID_ARG;
+  if (doc && (!causal || (reinterpret_cast<uintptr_t>(doc) & 3u) != 0))
+    return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
-void set_window(Shape* s, int window) { s->window = window >= s->N ? 0 : window; }
+void set_mask(Shape* s, int window, const int* doc) {
+  s->window = window >= s->N ? 0 : window;
+  s->doc = doc;
+}
 
 bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
 
@@ -106,7 +114,8 @@ int check_workspace(const void* ws, size_t bytes, const Shape& s) {
 size_t workspace_bytes(const Shape& s) {
   const size_t vec = round256(sizeof(float) * size_t(s.BH) * s.Npad);
   const size_t acc = round256(sizeof(float) * size_t(s.BH) * s.Npad * s.d);
-  return 2 * vec + acc;
+  const size_t items = round256(sizeof(int2) * size_t(s.BH) * s.n_tiles);
+  return 2 * vec + acc + items;
 }
 
 Workspace carve_workspace(void* base, const Shape& s) {
@@ -116,6 +125,8 @@ Workspace carve_workspace(void* base, const Shape& s) {
   w.L2 = reinterpret_cast<float*>(p);
   w.D = reinterpret_cast<float*>(p + vec);
   w.acc = reinterpret_cast<float*>(p + 2 * vec);
+  w.items = reinterpret_cast<int2*>(p + 2 * vec +
+                                    round256(sizeof(float) * size_t(s.BH) * s.Npad * s.d));
   return w;
 }
 
@@ -147,20 +158,9 @@ int make_acc_map(CUtensorMap* map, const float* acc, const Shape& s) {
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
-// attn_bwd_main with a sliding window (0 = none).
-int bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
-             int B, int H, int N, int d, int causal, int window, float scale, void* workspace,
-             size_t workspace_bytes_, void* stream) {
-  Shape s;
-  bool empty = false;
-  int st = make_shape(B, H, N, d, causal, &s, &empty);
-  if (st != ATTN_OK) return st;
-  if ((st = check_window(causal, window)) != ATTN_OK) return st;
-  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
-  if (empty) return ATTN_OK;
-  set_window(&s, window);
-  if ((st = check_ptrs({Q, K, V, dO, dK, dV})) != ATTN_OK) return st;
-  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+// The main kernel for a validated, non-empty shape (mask included).
+int bwd_main_launch(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                    void* dV, const Shape& s, float scale, void* workspace, void* stream) {
   int* err = error_word_ptr();
   if (!err) return ATTN_ERR_CUDA;
   const Workspace ws = carve_workspace(workspace, s);
@@ -204,19 +204,20 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
 
 int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N,
              int d, int causal, float scale, void* stream) {
-  return attn_fwd_ex(Q, K, V, O, L, B, H, N, d, causal, 0, scale, stream);
+  return attn_fwd_ex(Q, K, V, O, L, B, H, N, d, causal, 0, nullptr, scale, stream);
 }
 
 int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
-                int N, int d, int causal, int window, float scale, void* stream) {
+                int N, int d, int causal, int window, const int* doc_start, float scale,
+                void* stream) {
   Shape s;
   bool empty = false;
   int st = make_shape(B, H, N, d, causal, &s, &empty);
   if (st != ATTN_OK) return st;
-  if ((st = check_window(causal, window)) != ATTN_OK) return st;
+  if ((st = check_mask(causal, window, doc_start)) != ATTN_OK) return st;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
   if (empty) return ATTN_OK;
-  set_window(&s, window);
+  set_mask(&s, window, doc_start);
   if ((st = check_ptrs({Q, K, V, O, L})) != ATTN_OK) return st;
   int* err = error_word_ptr();
   if (!err) return ATTN_ERR_CUDA;
@@ -242,8 +243,15 @@ int attn_bwd_preprocess(const void* O, const void* dO, const float* L, int B, in
 int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dK, void* dV,
                   int B, int H, int N, int d, int causal, float scale, void* workspace,
                   size_t workspace_bytes_, void* stream) {
-  return bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, causal, 0, scale, workspace, workspace_bytes_,
-                  stream);
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q, K, V, dO, dK, dV})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  return bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, stream);
 }
 
 int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
@@ -263,29 +271,31 @@ int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const
 int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
              const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal,
              float scale, void* workspace, size_t workspace_bytes_, void* stream) {
-  return attn_bwd_ex(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, causal, 0, scale, workspace,
-                     workspace_bytes_, stream);
+  return attn_bwd_ex(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, causal, 0, nullptr, scale,
+                     workspace, workspace_bytes_, stream);
 }
 
 int attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
-                int causal, int window, float scale, void* workspace, size_t workspace_bytes_,
-                void* stream) {
+                int causal, int window, const int* doc_start, float scale, void* workspace,
+                size_t workspace_bytes_, void* stream) {
   Shape s;
   bool empty = false;
   int st = make_shape(B, H, N, d, causal, &s, &empty);
   if (st != ATTN_OK) return st;
-  if ((st = check_window(causal, window)) != ATTN_OK) return st;
+  if ((st = check_mask(causal, window, doc_start)) != ATTN_OK) return st;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
   if (empty) return ATTN_OK;
+  set_mask(&s, window, doc_start);
   if ((st = check_ptrs({Q, K, V, O, dO, L, dQ, dK, dV})) != ATTN_OK) return st;
   if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
-  st = attn_bwd_preprocess(O, dO, L, B, H, N, d, workspace, workspace_bytes_, stream);
-  if (st != ATTN_OK) return st;
-  st = bwd_main(Q, K, V, dO, dK, dV, B, H, N, d, causal, window, scale, workspace,
-                workspace_bytes_, stream);
-  if (st != ATTN_OK) return st;
-  return attn_bwd_dq_convert(dQ, B, H, N, d, scale, workspace, workspace_bytes_, stream);
+  const Workspace ws = carve_workspace(workspace, s);
+  if ((st = cuda_status(launch_bwd_preprocess(O, dO, L, ws, s, (cudaStream_t)stream))) !=
+      ATTN_OK)
+    return st;
+  if ((st = bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, stream)) != ATTN_OK)
+    return st;
+  return cuda_status(launch_bwd_dq_convert(dQ, ws, s, scale, (cudaStream_t)stream));
 }
 
 int attn_device_error_word(void* stream, int* word) {

@@ -41,6 +41,7 @@
 // is a handful of instructions per tile and runs on the copy engine.
 
 #include "kernels.h"
+#include "mask.cuh"
 #include "ptx.cuh"
 
 namespace attn {
@@ -134,7 +135,7 @@ struct Layout {
 // within a block and 16 KB across blocks; an MN-major operand advances 2 KB
 // (16 rows) per k-step, its MN extent spanning blocks 16 KB apart (LBO).
 
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, bool CAUSAL, int MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -143,11 +144,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmAcc, const float* __restrict__ L2ws,
                          const float* __restrict__ Dws,
                          __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int BH,
-                         int N, int head_group, int window_arg, float scale, float scale_log2,
+                         int N, int head_group, int window_arg, const int* __restrict__ doc,
+                         int H, const int2* __restrict__ items, float scale, float scale_log2,
                          int* err) {
-  // The sliding window has its own instantiation; without it the window code
-  // compiles away.
-  const int window = WINDOW ? window_arg : 0;
+  // The window and document masks have their own instantiations; without
+  // them their code compiles away.
+  const int window = MASK != kMaskPlain ? window_arg : 0;
   using Ly = Layout<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -165,8 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Query tiles of the item with key/value tile jt: it0 .. it0 + n_it - 1.
   // Under the causal mask they start at the diagonal; under a sliding window
   // they end at the last query that still sees a key of the tile,
-  // jt * 128 + 127 + window - 1.
-  auto item_tiles = [&](int jt) {
+  // jt * 128 + 127 + window - 1; with documents the preprocessing step has
+  // tabulated where they end (read only after griddepcontrol.wait).
+  auto item_tiles = [&](int jt, int bh) {
+    if (MASK == kMaskDocument) {
+      const int last = items[size_t(bh) * n_tiles + jt].x;
+      return (last < jt ? jt : (last >= n_tiles ? n_tiles - 1 : last)) - jt + 1;
+    }
     int last = n_tiles - 1;
     if (CAUSAL && window > 0) {
       const int lq = (jt * 128 + 126 + window) >> 7;
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
       imap.decode(item, jt, bh);
-      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt);
+      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt, bh);
       const int next = snake_item(k + 1, b, G, n_items);
       int njt = 0, nbh = 0;
       if (next >= 0) imap.decode(next, njt, nbh);
@@ -337,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
-      int jt, bh_unused;
-      imap.decode(item, jt, bh_unused);
-      const int n_it = item_tiles(jt);
+      int jt, bh;
+      imap.decode(item, jt, bh);
+      const int n_it = item_tiles(jt, bh);
       if (!(ok = mbar_wait_warp(bar(kBarKFull), k & 1, ctx, 0x220))) break;
       if (!(ok = mbar_wait_warp(bar(kBarQFull + (g & 1)), (g >> 1) & 1, ctx, 0x221))) break;
       tc_fence_after();
@@ -452,7 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
       imap.decode(item, jt, bh);
-      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt);
+      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt, bh);
+      const int* docb = MASK == kMaskDocument ? doc + size_t(bh / H) * N : nullptr;
+      const int doc_edge = MASK == kMaskDocument ? items[size_t(bh) * n_tiles + jt].y : n_tiles;
       for (int it = 0; it < n_it; ++it, ++g) {
         const int s = g & 1, qt = it0 + it;
         if (!(ok = mbar_wait_warp(bar(kBarQFull + s), (g >> 1) & 1, ctx, 0x230))) break;
@@ -473,7 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // sliding window: query column q of this tile sees key row r only
           // while (qt - jt) * 128 + q - r < window
           const int dq_tile = (qt - jt) * 128;
-          const bool wedge = CAUSAL && window > 0 && dq_tile + 127 >= window;
+          const bool wedge = MASK == kMaskWindow && CAUSAL && window > 0 && dq_tile + 127 >= window;
+          // documents (and a window with them): from the tabulated first query
+          // tile on, some query columns cannot see every key of the tile
+          const bool dedge = MASK == kMaskDocument && qt >= doc_edge;
           const float4* L2v4 = reinterpret_cast<const float4*>(L2v);
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
@@ -495,6 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (dq0 + 1 >= window) p1 = 0.f;
               if (dq0 + 2 >= window) p2 = 0.f;
               if (dq0 + 3 >= window) p3 = 0.f;
+            }
+            if (dedge) {  // key jt*128 + r is visible to query q from its first visible key on
+              const int q0 = qt * 128 + 64 * h + 4 * c4, kg = jt * 128 + r;
+              if (kg < first_visible_key(q0, docb, window, N)) p0 = 0.f;
+              if (kg < first_visible_key(q0 + 1, docb, window, N)) p1 = 0.f;
+              if (kg < first_visible_key(q0 + 2, docb, window, N)) p2 = 0.f;
+              if (kg < first_visible_key(q0 + 3, docb, window, N)) p3 = 0.f;
             }
             pk[2 * c4] = pack_bf16x2(p0, p1);
             pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
@@ -582,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
       imap.decode(item, jt, bh);
-      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt);
+      const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt, bh);
       for (int it = 0; it < n_it; ++it, ++g) {
         const int qt = it0 + it;
         // The four drain warps agree before any named barrier below, so that a
@@ -666,7 +685,8 @@ __global__ void __launch_bounds__(256)
                                const __nv_bfloat16* __restrict__ dO, const float* __restrict__ L,
                                float* __restrict__ L2ws, float* __restrict__ Dws,
                                float* __restrict__ acc, int BH, int N, int Npad,
-                               size_t acc_vec4) {
+                               size_t acc_vec4, const int* __restrict__ doc, int H, int window,
+                               int2* __restrict__ items) {
   constexpr int TPR = HD / 8;  // threads per row
   const size_t rows = size_t(BH) * Npad;
   const size_t units = rows * TPR;
@@ -714,6 +734,37 @@ __global__ void __launch_bounds__(256)
   }
   float4* a4 = reinterpret_cast<float4*>(acc);
   for (size_t i = gt; i < acc_vec4; i += nthreads) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // With documents: for key/value tile jt of head bh, the last query tile
+  // whose first row still sees a key of the tile, and the first query tile
+  // whose last row does not see the tile's first key (from there on the
+  // main kernel masks element-wise).  Row lower bounds never decrease, so
+  // both are binary searches over query tiles.
+  if (doc) {
+    const int n_tiles = Npad >> 7;
+    for (size_t i = gt; i < size_t(BH) * n_tiles; i += nthreads) {
+      const int bh = int(i / n_tiles), jt = int(i % n_tiles);
+      const int* docb = doc + size_t(bh / H) * N;
+      int a = jt, z = n_tiles - 1;
+      while (a < z) {
+        const int mid = (a + z + 1) >> 1;
+        if (first_visible_key(mid * 128, docb, window, N) <= jt * 128 + 127)
+          a = mid;
+        else
+          z = mid - 1;
+      }
+      const int last = a;
+      int e0 = jt, e1 = last + 1;
+      while (e0 < e1) {
+        const int mid = (e0 + e1) >> 1;
+        const int qlast = mid * 128 + 127 < N - 1 ? mid * 128 + 127 : N - 1;
+        if (first_visible_key(qlast, docb, window, N) > jt * 128)
+          e1 = mid;
+        else
+          e0 = mid + 1;
+      }
+      items[i] = make_int2(last, e0);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ step 3
@@ -813,15 +864,15 @@ static int head_group(const Shape& s) {
   return int(hg);
 }
 
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, bool CAUSAL, int MASK>
 static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                  const CUtensorMap& tmAcc, void* dK, void* dV,
                                  const Workspace& ws, const Shape& s, float scale, int* err,
                                  cudaStream_t stream) {
   using Ly = Layout<HD>;
-  auto kern = attn_bwd_main_kernel<HD, CAUSAL, WINDOW>;
-  cudaError_t e = set_smem_limit_once<attn_bwd_main_kernel<HD, CAUSAL, WINDOW>>(Ly::kBytes);
+  auto kern = attn_bwd_main_kernel<HD, CAUSAL, MASK>;
+  cudaError_t e = set_smem_limit_once<attn_bwd_main_kernel<HD, CAUSAL, MASK>>(Ly::kBytes);
   if (e != cudaSuccess) return e;
   // Persistent grid: at most one CTA per SM, each walking its work items.
   const long long n_items = (long long)s.n_tiles * s.BH;
@@ -829,7 +880,7 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV, tmdO, tmAcc,
                        ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
                        reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, head_group(s), s.window,
-                       scale,
+                       s.doc, s.H, static_cast<const int2*>(ws.items), scale,
                        scale * 1.4426950408889634f, err);
 }
 
@@ -852,27 +903,30 @@ cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
   auto g = reinterpret_cast<const __nv_bfloat16*>(dO);
   auto kern = s.d == 64 ? bwd::attn_bwd_preprocess_kernel<64> : bwd::attn_bwd_preprocess_kernel<128>;
   return launch_kernel(kern, dim3(grid), dim3(256), 0, stream, o, g, L, ws.L2, ws.D, ws.acc, s.BH,
-                       s.N, s.Npad, acc_vec4);
+                       s.N, s.Npad, acc_vec4, s.doc, s.H, s.window, ws.items);
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO,
                             const CUtensorMap& tmAcc, void* dK, void* dV, const Workspace& ws,
                             const Shape& s, float scale, int* err, cudaStream_t stream) {
-  const bool w = s.causal && s.window > 0;
-  if (s.d == 64)
-    return w ? bwd::launch_main_t<64, true, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s, scale,
-                                                  err, stream)
-           : s.causal ? bwd::launch_main_t<64, true, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws,
-                                                            s, scale, err, stream)
-                      : bwd::launch_main_t<64, false, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV,
-                                                             ws, s, scale, err, stream);
-  return w ? bwd::launch_main_t<128, true, true>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s, scale,
-                                                 err, stream)
-         : s.causal ? bwd::launch_main_t<128, true, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws,
-                                                           s, scale, err, stream)
-                    : bwd::launch_main_t<128, false, false>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV,
-                                                            ws, s, scale, err, stream);
+  const int mask = !s.causal ? kMaskPlain
+                   : s.doc        ? kMaskDocument
+                   : s.window > 0 ? kMaskWindow
+                                  : kMaskPlain;
+#define ATTN_MAIN(HD_, C_, M_) \
+  bwd::launch_main_t<HD_, C_, M_>(tmQ, tmK, tmV, tmdO, tmAcc, dK, dV, ws, s, scale, err, stream)
+  if (s.d == 64) {
+    if (!s.causal) return ATTN_MAIN(64, false, kMaskPlain);
+    if (mask == kMaskDocument) return ATTN_MAIN(64, true, kMaskDocument);
+    if (mask == kMaskWindow) return ATTN_MAIN(64, true, kMaskWindow);
+    return ATTN_MAIN(64, true, kMaskPlain);
+  }
+  if (!s.causal) return ATTN_MAIN(128, false, kMaskPlain);
+  if (mask == kMaskDocument) return ATTN_MAIN(128, true, kMaskDocument);
+  if (mask == kMaskWindow) return ATTN_MAIN(128, true, kMaskWindow);
+  return ATTN_MAIN(128, true, kMaskPlain);
+#undef ATTN_MAIN
 }
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,

@@ -26,6 +26,7 @@
 //    records an error, drains the tensor core and exits normally.
 
 #include "kernels.h"
+#include "mask.cuh"
 #include "ptx.cuh"
 
 namespace attn {
@@ -72,15 +73,15 @@ struct Layout {
 // within a block and 16 KB across blocks; an MN-major operand advances 2 KB
 // (16 rows) per k-step, its MN extent spanning blocks 16 KB apart (LBO).
 
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, bool CAUSAL, int MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
                     float* __restrict__ Lout, int BH, int N, float scale_log2, int window_arg,
-                    int* err) {
-  // The sliding window has its own instantiation; without it the window code
-  // compiles away.
-  const int window = WINDOW ? window_arg : 0;
+                    const int* __restrict__ doc, int H, int* err) {
+  // The window and document masks have their own instantiations; without
+  // them their code compiles away.
+  const int window = MASK != kMaskPlain ? window_arg : 0;
   using Ly = Layout<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -106,9 +107,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tiles wholly below that are skipped (tile B's extra leading tiles are
   // masked for its rows).
   const int kv_end = CAUSAL ? min(n_tiles, qt_a + (has_b ? 2 : 1)) : n_tiles;
+  // With documents, the first row's document start also bounds it (read
+  // below, once the previous kernel has finished: the map may be its output).
   const int lo_key = qt_a * 128 - window + 1;
-  const int kv_lo = (CAUSAL && window > 0 && lo_key > 0) ? lo_key / 128 : 0;
-  const int n_kv = kv_end - kv_lo;
+  int kv_lo = (CAUSAL && window > 0 && lo_key > 0) ? lo_key / 128 : 0;
+  int n_kv = kv_end - kv_lo;
+  const int* docb = MASK == kMaskDocument ? doc + size_t(bh / H) * N : nullptr;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
@@ -148,6 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Everything above overlaps the previous kernel; its results are read below.
   grid_dep_wait();
   grid_dep_launch();
+  if (MASK == kMaskDocument) {  // row lower bounds never decrease along the tile pair
+    kv_lo = first_visible_key(qt_a * 128, docb, window, N) / 128;
+    n_kv = kv_end - kv_lo;
+  }
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -269,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tO = tbase + lane_off + Ly::kColO + HD * t;
       const int q_tile0 = (qt_a + t) * 128;
       const int q = q_tile0 + r;
+      // first key this row may see (window, document)
+      const int lo_q = MASK != kMaskPlain ? first_visible_key(q, docb, window, N) : 0;
       float m = -INFINITY;  // running max of the base-2 scaled scores
       float l = 0.f;        // running sum of 2^(x - m)
       bool ok = true;
@@ -282,14 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
         tmem_wait_ld();
         const int kv0 = (kv_lo + j) * 128;
-        // masked: above the diagonal, beyond N, or (sliding window) at least
-        // `window` keys behind the query
-        const bool below = CAUSAL && window > 0 && kv0 <= q_tile0 + 127 - window;
+        // masked: above the diagonal, beyond N, or before the first key the
+        // row may see (sliding window, document)
+        const bool below = MASK != kMaskPlain && kv0 < lo_q;
         if ((CAUSAL && kv0 + 127 > q_tile0) || kv0 + 128 > N || below) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int kv = kv0 + c;
-            if ((CAUSAL && kv > q) || kv >= N || (below && q - kv >= window))
+            if ((CAUSAL && kv > q) || kv >= N || (below && kv < lo_q))
               u[c] = __float_as_uint(-INFINITY);
           }
         }
@@ -380,20 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD, bool CAUSAL, bool WINDOW>
+template <int HD, bool CAUSAL, int MASK>
 static cudaError_t launch_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, void* O, float* L, const Shape& s,
                             float scale, int* err, cudaStream_t stream) {
   using Ly = Layout<HD>;
-  auto kern = attn_fwd_kernel<HD, CAUSAL, WINDOW>;
-  cudaError_t e = set_smem_limit_once<attn_fwd_kernel<HD, CAUSAL, WINDOW>>(Ly::kBytes);
+  auto kern = attn_fwd_kernel<HD, CAUSAL, MASK>;
+  cudaError_t e = set_smem_limit_once<attn_fwd_kernel<HD, CAUSAL, MASK>>(Ly::kBytes);
   if (e != cudaSuccess) return e;
   const int n_pairs = (s.n_tiles + 1) / 2;
   const dim3 grid(unsigned(n_pairs) * unsigned(s.BH));
   const float scale_log2 = scale * 1.4426950408889634f;
   return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV,
                        reinterpret_cast<__nv_bfloat16*>(O), L, s.BH, s.N, scale_log2, s.window,
-                       err);
+                       s.doc, s.H, err);
 }
 
 }  // namespace fwd
@@ -401,15 +411,24 @@ static cudaError_t launch_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
 cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        void* O, float* L, const Shape& s, float scale, int* err,
                        cudaStream_t stream) {
-  if (s.d == 64)
-    return s.causal && s.window > 0
-               ? fwd::launch_t<64, true, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
-           : s.causal ? fwd::launch_t<64, true, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
-                      : fwd::launch_t<64, false, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
-  return s.causal && s.window > 0
-             ? fwd::launch_t<128, true, true>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
-         : s.causal ? fwd::launch_t<128, true, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream)
-                    : fwd::launch_t<128, false, false>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+  const int mask = !s.causal ? kMaskPlain
+                   : s.doc        ? kMaskDocument
+                   : s.window > 0 ? kMaskWindow
+                                  : kMaskPlain;
+  if (s.d == 64) {
+    if (!s.causal) return fwd::launch_t<64, false, kMaskPlain>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+    if (mask == kMaskDocument)
+      return fwd::launch_t<64, true, kMaskDocument>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+    if (mask == kMaskWindow)
+      return fwd::launch_t<64, true, kMaskWindow>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+    return fwd::launch_t<64, true, kMaskPlain>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+  }
+  if (!s.causal) return fwd::launch_t<128, false, kMaskPlain>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+  if (mask == kMaskDocument)
+    return fwd::launch_t<128, true, kMaskDocument>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+  if (mask == kMaskWindow)
+    return fwd::launch_t<128, true, kMaskWindow>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
+  return fwd::launch_t<128, true, kMaskPlain>(tmQ, tmK, tmV, O, L, s, scale, err, stream);
 }
 
 }  // namespace attn

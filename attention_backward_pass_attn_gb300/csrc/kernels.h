@@ -22,16 +22,23 @@ struct Shape {
   int Npad;     // n_tiles * 128
   int window;   // causal sliding window: key j visible to query i iff i - window < j <= i;
                 // 0 = no window (also used for window >= N)
+  int H;        // heads per batch element (BH = B * H)
+  const int* doc;  // causal documents: doc[b * N + i] = first position of i's document,
+                   // device memory; null = none
 };
 
-// Workspace carve-up (all fp32, 256-byte aligned sections):
-//   L2  [BH][Npad]            L * log2(e); +inf on padded rows
-//   D   [BH][Npad]            rowsum(dO o O); 0 on padded rows
-//   acc [BH][Npad][d]         dQ accumulator (unscaled), row-major
+// Workspace carve-up (256-byte aligned sections):
+//   L2    [BH][Npad]     fp32  L * log2(e); +inf on padded rows
+//   D     [BH][Npad]     fp32  rowsum(dO o O); 0 on padded rows
+//   acc   [BH][Npad][d]  fp32  dQ accumulator (unscaled), row-major
+//   items [BH][n_tiles]  int2  with documents: per key/value tile, the last
+//                              query tile that sees it and the first query
+//                              tile that needs element-wise masking
 struct Workspace {
   float* L2;
   float* D;
   float* acc;
+  int2* items;
 };
 
 // Launches a kernel of this library with programmatic dependent launch

@@ -71,22 +71,35 @@ int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int
              int N, int d, int causal, float scale, void* stream);
 
 /*
- * Forward with a causal sliding window: key j is visible to query i when
- * i - window < j <= i, so each query sees itself and the window - 1 keys
- * before it (the banded causal mask of sliding-window attention, named in
- * "Training - CUDA Moat Still Alive", section on attention variants, for
- * Mistral 7B).  window = 0 means no window, and window >= N is the plain
- * causal mask; otherwise as attn_fwd.  A window requires causal = 1 (else
- * ATTN_ERR_INVALID_ARG, as for a negative window).  Key/value tiles wholly
- * outside the band are skipped, so the cost grows with N * window, not N^2.
+ * Forward with the mask variants of "Training - CUDA Moat Still Alive",
+ * section on attention variants, on top of the causal mask; otherwise as
+ * attn_fwd.
+ *
+ *   window     sliding window (Mistral 7B): key j is visible to query i
+ *              when i - window < j <= i.  0 = none; window >= N is the
+ *              causal mask.
+ *   doc_start  document mask for packed sequences (FlexAttention's document
+ *              mask): DEVICE int32 [B][N], doc_start[b*N + i] = the first
+ *              position of the document holding position i, so query i sees
+ *              keys doc_start[i] <= j <= i.  NULL = one document.  Entries
+ *              must be i (a document starts) or doc_start[i - 1]; other
+ *              values give unspecified results (no fault).  4-byte aligned.
+ *
+ * Both need causal = 1 (else ATTN_ERR_INVALID_ARG, as for a negative window)
+ * and combine: j >= max(doc_start[i], i - window + 1).  Key/value tiles that
+ * no query of a tile can see are skipped, so the cost follows the visible
+ * area (N * window, or the sum of squared document lengths), not N^2.
  */
 int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
-                int N, int d, int causal, int window, float scale, void* stream);
+                int N, int d, int causal, int window, const int* doc_start, float scale,
+                void* stream);
 
 /*
  * Bytes of device workspace attn_bwd needs for this shape (0 for an empty
  * problem).  Holds, per head, D = rowsum(dO o O) and L scaled to base 2, each
- * [roundup(N,128)] fp32, and an fp32 dQ accumulator of roundup(N,128) x d.
+ * [roundup(N,128)] fp32, an fp32 dQ accumulator of roundup(N,128) x d, and
+ * two int32 per 128-row tile (query ranges under a document mask); each
+ * section starts on a 256-byte boundary.
  * The workspace must be 256-byte aligned; its contents on entry do not matter.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);
@@ -105,14 +118,14 @@ int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const v
              int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Backward with a causal sliding window (see attn_fwd_ex); L must come from
- * attn_fwd_ex with the same window.  Same workspace and steps as attn_bwd;
- * window = 0 is attn_bwd.
+ * Backward with the mask variants of attn_fwd_ex (window, doc_start; L must
+ * come from attn_fwd_ex with the same mask).  Same workspace and steps as
+ * attn_bwd; window = 0 and doc_start = NULL is attn_bwd.
  */
 int attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
-                int causal, int window, float scale, void* workspace, size_t workspace_bytes,
-                void* stream);
+                int causal, int window, const int* doc_start, float scale, void* workspace,
+                size_t workspace_bytes, void* stream);
 
 /*
  * Step 1 of attn_bwd: D_i = <dO_i, O_i> in fp32 and L_i * log2(e) into the

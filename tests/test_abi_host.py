@@ -57,11 +57,12 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # D and L2: BH*Npad fp32 each; acc: BH*Npad*d fp32; each section 256-aligned
+    # D and L2: BH*Npad fp32 each; acc: BH*Npad*d fp32; two int32 per tile for
+    # document ranges; each section 256-aligned
     def expect(B, H, N, d):
         npad = (N + 127) // 128 * 128
         r = lambda x: (x + 255) // 256 * 256
-        return 2 * r(4 * B * H * npad) + r(4 * B * H * npad * d)
+        return 2 * r(4 * B * H * npad) + r(4 * B * H * npad * d) + r(8 * B * H * (npad // 128))
     for args in ((1, 2, 128, 64), (2, 16, 2048, 64), (1, 3, 129, 128), (4, 16, 8192, 128)):
         assert lib.attn_bwd_workspace_size(*args) == expect(*args)
     assert lib.attn_bwd_workspace_size(0, 2, 128, 64) == 0
@@ -128,19 +129,24 @@ def test_bwd_validation(lib):
 def test_window_validation(lib):
     """The sliding window is causal only and non-negative; checked before
     anything else is looked at, empty problems included."""
-    def fwd_ex(causal, window, N=128, ptr=FAKE):
-        return lib.attn_fwd_ex(ptr, ptr, ptr, ptr, ptr, 1, 1, N, 64, causal, window, 0.125, None)
+    def fwd_ex(causal, window, N=128, ptr=FAKE, doc=None):
+        return lib.attn_fwd_ex(ptr, ptr, ptr, ptr, ptr, 1, 1, N, 64, causal, window, doc, 0.125,
+                               None)
 
-    def bwd_ex(causal, window, N=128, ptr=FAKE):
+    def bwd_ex(causal, window, N=128, ptr=FAKE, doc=None):
         need = lib.attn_bwd_workspace_size(1, 1, max(N, 0), 64)
         return lib.attn_bwd_ex(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, N, 64, causal,
-                               window, 0.125, FAKE, need, None)
+                               window, doc, 0.125, FAKE, need, None)
     for f in (fwd_ex, bwd_ex):
         assert f(0, 16) == ab.ATTN_ERR_INVALID_ARG
         assert f(1, -1) == ab.ATTN_ERR_INVALID_ARG
         assert f(0, 16, N=0, ptr=None) == ab.ATTN_ERR_INVALID_ARG
         assert f(1, 16, N=0, ptr=None) == ab.ATTN_OK
         assert f(1, 16, ptr=None) == ab.ATTN_ERR_INVALID_ARG  # null pointers still rejected
+        # document maps: causal only, 4-byte aligned
+        assert f(0, 0, doc=FAKE) == ab.ATTN_ERR_INVALID_ARG
+        assert f(1, 0, doc=FAKE + 2) == ab.ATTN_ERR_INVALID_ARG
+        assert f(1, 0, N=0, ptr=None, doc=FAKE) == ab.ATTN_OK
 
 
 def test_binding_checks_tensors():
