@@ -115,7 +115,8 @@ size_t workspace_bytes(const Shape& s) {
   const size_t vec = round256(sizeof(float) * size_t(s.BH) * s.Npad);
   const size_t acc = round256(sizeof(float) * size_t(s.BH) * s.Npad * s.d);
   const size_t items = round256(sizeof(int2) * size_t(s.BH) * s.n_tiles);
-  return 2 * vec + acc + items;
+  const size_t order = round256(sizeof(int) * size_t(s.BH) * s.n_tiles);
+  return 3 * vec + acc + items + order;  // qend: one int32 per row, the size of a vec section
 }
 
 Workspace carve_workspace(void* base, const Shape& s) {
@@ -125,8 +126,11 @@ Workspace carve_workspace(void* base, const Shape& s) {
   w.L2 = reinterpret_cast<float*>(p);
   w.D = reinterpret_cast<float*>(p + vec);
   w.acc = reinterpret_cast<float*>(p + 2 * vec);
-  w.items = reinterpret_cast<int2*>(p + 2 * vec +
-                                    round256(sizeof(float) * size_t(s.BH) * s.Npad * s.d));
+  char* q = p + 2 * vec + round256(sizeof(float) * size_t(s.BH) * s.Npad * s.d);
+  w.items = reinterpret_cast<int2*>(q);
+  w.qend = reinterpret_cast<int*>(q + round256(sizeof(int2) * size_t(s.BH) * s.n_tiles));
+  w.order = reinterpret_cast<int*>(reinterpret_cast<char*>(w.qend) +
+                                   round256(sizeof(int) * size_t(s.BH) * s.Npad));
   return w;
 }
 
@@ -292,6 +296,8 @@ int attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, cons
   const Workspace ws = carve_workspace(workspace, s);
   if ((st = cuda_status(launch_bwd_preprocess(O, dO, L, ws, s, (cudaStream_t)stream))) !=
       ATTN_OK)
+    return st;
+  if (s.doc && (st = cuda_status(launch_bwd_order(ws, s, (cudaStream_t)stream))) != ATTN_OK)
     return st;
   if ((st = bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, stream)) != ATTN_OK)
     return st;

@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const float* __restrict__ Dws,
                          __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int BH,
                          int N, int head_group, int window_arg, const int* __restrict__ doc,
-                         int H, const int2* __restrict__ items, float scale, float scale_log2,
+                         int H, const int2* __restrict__ items, const int* __restrict__ qend,
+                         const int* __restrict__ order, float scale, float scale_log2,
                          int* err) {
   // The window and document masks have their own instantiations; without
   // them their code compiles away.
@@ -164,6 +165,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Npad = n_tiles * 128;
   const int n_items = BH * n_tiles;
   const ItemMap imap{BH, n_tiles, head_group};
+  // With documents the items come from the sorted list (heaviest first).
+  auto decode_item = [&](int idx, int& jt, int& bh) {
+    if (MASK == kMaskDocument) {
+      const int id = order[idx];
+      bh = id / n_tiles;
+      jt = id - bh * n_tiles;
+    } else {
+      imap.decode(idx, jt, bh);
+    }
+  };
   // Query tiles of the item with key/value tile jt: it0 .. it0 + n_it - 1.
   // Under the causal mask they start at the diagonal; under a sliding window
   // they end at the last query that still sees a key of the tile,
@@ -244,11 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
-      imap.decode(item, jt, bh);
+      decode_item(item, jt, bh);
       const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt, bh);
       const int next = snake_item(k + 1, b, G, n_items);
       int njt = 0, nbh = 0;
-      if (next >= 0) imap.decode(next, njt, nbh);
+      if (next >= 0) decode_item(next, njt, nbh);
       if (k > 0 && !(ok = mbar_wait_warp(bar(kBarVEmpty), (k - 1) & 1, ctx, 0x212))) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(bar(kBarVFull), Ly::kTileBytes);
@@ -345,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
-      imap.decode(item, jt, bh);
+      decode_item(item, jt, bh);
       const int n_it = item_tiles(jt, bh);
       if (!(ok = mbar_wait_warp(bar(kBarKFull), k & 1, ctx, 0x220))) break;
       if (!(ok = mbar_wait_warp(bar(kBarQFull + (g & 1)), (g >> 1) & 1, ctx, 0x221))) break;
@@ -458,10 +469,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
-      imap.decode(item, jt, bh);
+      decode_item(item, jt, bh);
       const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt, bh);
-      const int* docb = MASK == kMaskDocument ? doc + size_t(bh / H) * N : nullptr;
       const int doc_edge = MASK == kMaskDocument ? items[size_t(bh) * n_tiles + jt].y : n_tiles;
+      // with documents: this thread's key jt*128 + r is seen by queries below
+      // q_lim only (the end of its document, and of the window)
+      int q_lim = N;
+      if (MASK == kMaskDocument) {
+        const int kg = jt * 128 + r;
+        q_lim = qend[size_t(bh) * Npad + kg];
+        if (window > 0 && kg + window < q_lim) q_lim = kg + window;
+      }
       for (int it = 0; it < n_it; ++it, ++g) {
         const int s = g & 1, qt = it0 + it;
         if (!(ok = mbar_wait_warp(bar(kBarQFull + s), (g >> 1) & 1, ctx, 0x230))) break;
@@ -508,12 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (dq0 + 2 >= window) p2 = 0.f;
               if (dq0 + 3 >= window) p3 = 0.f;
             }
-            if (dedge) {  // key jt*128 + r is visible to query q from its first visible key on
-              const int q0 = qt * 128 + 64 * h + 4 * c4, kg = jt * 128 + r;
-              if (kg < first_visible_key(q0, docb, window, N)) p0 = 0.f;
-              if (kg < first_visible_key(q0 + 1, docb, window, N)) p1 = 0.f;
-              if (kg < first_visible_key(q0 + 2, docb, window, N)) p2 = 0.f;
-              if (kg < first_visible_key(q0 + 3, docb, window, N)) p3 = 0.f;
+            if (dedge) {  // query columns at or past q_lim cannot see this key
+              const int q0 = qt * 128 + 64 * h + 4 * c4;
+              if (q0 >= q_lim) p0 = 0.f;
+              if (q0 + 1 >= q_lim) p1 = 0.f;
+              if (q0 + 2 >= q_lim) p2 = 0.f;
+              if (q0 + 3 >= q_lim) p3 = 0.f;
             }
             pk[2 * c4] = pack_bf16x2(p0, p1);
             pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
@@ -600,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
       int jt, bh;
-      imap.decode(item, jt, bh);
+      decode_item(item, jt, bh);
       const int it0 = CAUSAL ? jt : 0, n_it = item_tiles(jt, bh);
       for (int it = 0; it < n_it; ++it, ++g) {
         const int qt = it0 + it;
@@ -686,7 +704,7 @@ __global__ void __launch_bounds__(256)
                                float* __restrict__ L2ws, float* __restrict__ Dws,
                                float* __restrict__ acc, int BH, int N, int Npad,
                                size_t acc_vec4, const int* __restrict__ doc, int H, int window,
-                               int2* __restrict__ items) {
+                               int2* __restrict__ items, int* __restrict__ qend) {
   constexpr int TPR = HD / 8;  // threads per row
   const size_t rows = size_t(BH) * Npad;
   const size_t units = rows * TPR;
@@ -763,6 +781,23 @@ __global__ void __launch_bounds__(256)
           e0 = mid + 1;
       }
       items[i] = make_int2(last, e0);
+    }
+    // Per key position k: one past the last query of k's document, the first
+    // position after k whose document starts after k (binary search; N if
+    // k's document runs to the end).  Queries from there on cannot see k.
+    for (size_t i = gt; i < size_t(BH) * Npad; i += nthreads) {
+      const int bh = int(i / Npad), k = int(i % Npad);
+      const int* docb = doc + size_t(bh / H) * N;
+      int a = k + 1, z = N;  // answer in [k + 1, N]
+      if (k >= N) a = z = N;
+      while (a < z) {
+        const int mid = (a + z) >> 1;
+        if (first_visible_key(mid, docb, 0, N) > k)
+          z = mid;
+        else
+          a = mid + 1;
+      }
+      qend[i] = a;
     }
   }
 }
@@ -880,7 +915,9 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV, tmdO, tmAcc,
                        ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
                        reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N, head_group(s), s.window,
-                       s.doc, s.H, static_cast<const int2*>(ws.items), scale,
+                       s.doc, s.H, static_cast<const int2*>(ws.items),
+                       static_cast<const int*>(ws.qend), static_cast<const int*>(ws.order),
+                       scale,
                        scale * 1.4426950408889634f, err);
 }
 
@@ -903,7 +940,7 @@ cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
   auto g = reinterpret_cast<const __nv_bfloat16*>(dO);
   auto kern = s.d == 64 ? bwd::attn_bwd_preprocess_kernel<64> : bwd::attn_bwd_preprocess_kernel<128>;
   return launch_kernel(kern, dim3(grid), dim3(256), 0, stream, o, g, L, ws.L2, ws.D, ws.acc, s.BH,
-                       s.N, s.Npad, acc_vec4, s.doc, s.H, s.window, ws.items);
+                       s.N, s.Npad, acc_vec4, s.doc, s.H, s.window, ws.items, ws.qend);
 }
 
 cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
@@ -927,6 +964,60 @@ cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   if (mask == kMaskWindow) return ATTN_MAIN(128, true, kMaskWindow);
   return ATTN_MAIN(128, true, kMaskPlain);
 #undef ATTN_MAIN
+}
+
+namespace bwd {
+
+// Counting sort of the work items by query-tile count, most first, in one CTA
+// (bucket counts in shared memory; counts at or above kOrderBins share the
+// last bucket, which only coarsens the order).
+constexpr int kOrderBins = 8192;
+
+__global__ void __launch_bounds__(1024)
+    attn_bwd_order_kernel(const int2* __restrict__ items, int n_tiles, int n_items,
+                          int* __restrict__ order) {
+  __shared__ int bins[kOrderBins];
+  __shared__ int partial[1024];
+  grid_dep_wait();  // the item table comes from the preprocessing step
+  grid_dep_launch();
+  auto weight = [&](int id) {
+    const int jt = id % n_tiles;
+    int w = items[id].x - jt + 1;
+    w = w < 1 ? 1 : (w >= kOrderBins ? kOrderBins - 1 : w);
+    return kOrderBins - 1 - w;  // heaviest in bucket 0
+  };
+  for (int i = threadIdx.x; i < kOrderBins; i += blockDim.x) bins[i] = 0;
+  __syncthreads();
+  for (int id = threadIdx.x; id < n_items; id += blockDim.x) atomicAdd(&bins[weight(id)], 1);
+  __syncthreads();
+  // exclusive prefix sum over the buckets: each thread sums a run of 8
+  constexpr int kRun = kOrderBins / 1024;
+  int run = 0;
+  for (int j = 0; j < kRun; ++j) run += bins[threadIdx.x * kRun + j];
+  partial[threadIdx.x] = run;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan of the run sums
+    const int v = threadIdx.x >= off ? partial[threadIdx.x - off] : 0;
+    __syncthreads();
+    partial[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int base = partial[threadIdx.x] - run;
+  for (int j = 0; j < kRun; ++j) {
+    const int c = bins[threadIdx.x * kRun + j];
+    bins[threadIdx.x * kRun + j] = base;
+    base += c;
+  }
+  __syncthreads();
+  for (int id = threadIdx.x; id < n_items; id += blockDim.x)
+    order[atomicAdd(&bins[weight(id)], 1)] = id;
+}
+
+}  // namespace bwd
+
+cudaError_t launch_bwd_order(const Workspace& ws, const Shape& s, cudaStream_t stream) {
+  return launch_kernel(bwd::attn_bwd_order_kernel, dim3(1), dim3(1024), 0, stream,
+                       static_cast<const int2*>(ws.items), s.n_tiles, s.BH * s.n_tiles, ws.order);
 }
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,

@@ -34,11 +34,17 @@ struct Shape {
 //   items [BH][n_tiles]  int2  with documents: per key/value tile, the last
 //                              query tile that sees it and the first query
 //                              tile that needs element-wise masking
+//   qend  [BH][Npad]     int32 with documents: per key, one past the last
+//                              query of its document
+//   order [BH*n_tiles]   int32 with documents: work items (bh * n_tiles + jt)
+//                              sorted by query-tile count, most first
 struct Workspace {
   float* L2;
   float* D;
   float* acc;
   int2* items;
+  int* qend;
+  int* order;
 };
 
 // Launches a kernel of this library with programmatic dependent launch
@@ -101,6 +107,11 @@ cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO,
                             const CUtensorMap& tmAcc, void* dK, void* dV, const Workspace& ws,
                             const Shape& s, float scale, int* err, cudaStream_t stream);
+
+// With documents: sorts the work items by their query-tile count (from the
+// preprocessing step's table) so that the main kernel deals them out heaviest
+// first.
+cudaError_t launch_bwd_order(const Workspace& ws, const Shape& s, cudaStream_t stream);
 
 cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s, float scale,
                                   cudaStream_t stream);

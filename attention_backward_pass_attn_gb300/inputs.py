@@ -33,6 +33,7 @@ class Workload:
     q_scale: float = 1.0   # Q is multiplied by this before the bf16 cast
     do_scale: float = 1.0  # dO is multiplied by this before the bf16 cast
     window: int = 0        # causal sliding window (0 = none)
+    doc_lengths: tuple = ()  # causal documents packed in order (empty = one document)
 
     @property
     def scale(self) -> float:
@@ -45,8 +46,11 @@ class Workload:
 
     def pairs(self) -> float:
         """Visible (query, key) pairs per head: N^2, N^2/2 under the causal
-        mask, and N*W - W^2/2 (the area of the band) under a window W < N."""
+        mask, N*W - W^2/2 (the area of the band) under a window W < N, and
+        the sum of n^2/2 over packed documents of lengths n."""
         N, W = float(self.N), float(self.window)
+        if self.causal and self.doc_lengths:
+            return sum(float(n) * n / 2 for n in self.doc_lengths)
         if self.causal and 0 < W < N:
             return N * W - W * W / 2
         return N * N / 2 if self.causal else N * N
@@ -84,12 +88,41 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
-# Sliding-window attention at the Mistral 7B window (4096 keys), measured
-# beside the workloads above.
+def _packed_lengths(N: int, lo: int, hi: int, seed: int) -> tuple:
+    """Document lengths drawn uniformly from [lo, hi] until N positions are
+    filled (the last one cut to fit): a seeded packing of variable-length
+    sequences."""
+    g = torch.Generator().manual_seed(seed)
+    out = []
+    while sum(out) < N:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g))
+        out.append(min(n, N - sum(out)))
+    return tuple(out)
+
+
+# Mask variants measured beside the workloads above: sliding-window attention
+# at the Mistral 7B window (4096 keys), and packed documents of 512 to 4096
+# positions.
 EXTRA_WORKLOADS = {
     "b1h16n16384d128_w4096": Workload("b1h16n16384d128_w4096", 1, 16, 16384, 128, True,
                                       seed=5, window=4096),
+    "b1h16n16384d128_docs": Workload("b1h16n16384d128_docs", 1, 16, 16384, 128, True, seed=6,
+                                     doc_lengths=_packed_lengths(16384, 512, 4096, seed=6)),
 }
+
+
+def make_doc_map(w: Workload) -> torch.Tensor | None:
+    """The document map of a workload, int32 [B, N] (the first position of
+    each position's document; the same packing for every batch element), or
+    None for one document."""
+    if not w.doc_lengths:
+        return None
+    starts = []
+    pos = 0
+    for n in w.doc_lengths:
+        starts.extend([pos] * n)
+        pos += n
+    return torch.tensor(starts, dtype=torch.int32).repeat(w.B, 1)
 
 
 def make_inputs(w: Workload, dtype=torch.bfloat16):

@@ -195,7 +195,7 @@ def time_workload(w, steps: int, warmup: int, flush, split=False):
     import torch
 
     from attention_backward_pass_attn_gb300 import binding as ab
-    from attention_backward_pass_attn_gb300.inputs import make_inputs
+    from attention_backward_pass_attn_gb300.inputs import make_doc_map, make_inputs
 
     dev = torch.device("cuda", torch.cuda.current_device())
     q, k, v, do = (t.to(dev) for t in make_inputs(w))
@@ -204,9 +204,12 @@ def time_workload(w, steps: int, warmup: int, flush, split=False):
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     ws = ab.alloc_workspace(w.B, w.H, w.N, w.d, dev)
     stream = torch.cuda.current_stream()
+    dmap = make_doc_map(w)
+    dmap = dmap.to(dev) if dmap is not None else None
 
     def step():
-        ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream, window=w.window)
+        ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream, window=w.window,
+                    doc=dmap)
         e[1].record(stream)
         if split:
             ab.attn_bwd_preprocess(o, do, lse, ws, stream=stream)
@@ -216,7 +219,7 @@ def time_workload(w, steps: int, warmup: int, flush, split=False):
             ab.attn_bwd_dq_convert(dq, ws, scale=w.scale, stream=stream)
         else:  # the public call: the same three kernels
             ab.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
-                        workspace=ws, stream=stream, window=w.window)
+                        workspace=ws, stream=stream, window=w.window, doc=dmap)
 
     rec = []
     for i in range(warmup + steps):
@@ -408,18 +411,20 @@ def run_ours(args):
                                     / statistics.median(r["fwd"]) / 1e9, 1),
                 "main_ms_median": round(mm, 4),
             }
-        # Sliding window (banded causal mask, 4096 keys): FLOPs are those of the
-        # visible band, N*W - W^2/2 pairs per head.
+        # Mask variants: a sliding window (4096 keys) and packed documents.
+        # FLOPs are those of the visible pairs: N*W - W^2/2 per head under the
+        # window, the sum of n^2/2 over documents of lengths n.
         for name, sw in EXTRA_WORKLOADS.items():
             rw = time_workload(sw, 10, 3, flush)
             extra[name] = {
                 "window": sw.window,
+                "documents": len(sw.doc_lengths),
                 "bwd_total_tflops": round(sw.bwd_flops() / statistics.median(rw["bwd"]) / 1e9, 1),
                 "bwd_total_frac": round(sw.bwd_flops() / statistics.median(rw["bwd"]) / 1e9
                                         / peak_tf, 4),
                 "fwd_tflops": round(sw.fwd_flops() / statistics.median(rw["fwd"]) / 1e9, 1),
                 "bwd_ms_median": round(statistics.median(rw["bwd"]), 4),
-                "flops": "10*d*(N*W - W^2/2) per head (backward), 4*d*(...) (forward)",
+                "flops": "10*d*(visible pairs) per head (backward), 4*d*(...) (forward)",
             }
 
     if rank != 0:

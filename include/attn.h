@@ -97,9 +97,10 @@ int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, 
 /*
  * Bytes of device workspace attn_bwd needs for this shape (0 for an empty
  * problem).  Holds, per head, D = rowsum(dO o O) and L scaled to base 2, each
- * [roundup(N,128)] fp32, an fp32 dQ accumulator of roundup(N,128) x d, and
- * two int32 per 128-row tile (query ranges under a document mask); each
- * section starts on a 256-byte boundary.
+ * [roundup(N,128)] fp32, an fp32 dQ accumulator of roundup(N,128) x d,
+ * three int32 per 128-row tile and one per row (query ranges and the order
+ * of work under a document mask); each section starts on a 256-byte
+ * boundary.
  * The workspace must be 256-byte aligned; its contents on entry do not matter.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);

@@ -57,12 +57,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # D and L2: BH*Npad fp32 each; acc: BH*Npad*d fp32; two int32 per tile for
-    # document ranges; each section 256-aligned
+    # D and L2: BH*Npad fp32 each; acc: BH*Npad*d fp32; two int32 per tile and
+    # one per row for document ranges; each section 256-aligned
     def expect(B, H, N, d):
         npad = (N + 127) // 128 * 128
         r = lambda x: (x + 255) // 256 * 256
-        return 2 * r(4 * B * H * npad) + r(4 * B * H * npad * d) + r(8 * B * H * (npad // 128))
+        return (3 * r(4 * B * H * npad) + r(4 * B * H * npad * d)
+                + r(8 * B * H * (npad // 128)) + r(4 * B * H * (npad // 128)))
     for args in ((1, 2, 128, 64), (2, 16, 2048, 64), (1, 3, 129, 128), (4, 16, 8192, 128)):
         assert lib.attn_bwd_workspace_size(*args) == expect(*args)
     assert lib.attn_bwd_workspace_size(0, 2, 128, 64) == 0
