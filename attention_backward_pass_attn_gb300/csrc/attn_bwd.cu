@@ -34,6 +34,16 @@
 // d = 64, one for d = 128), the dS^T
 // tile and two 16 KB fp32 staging buffers for the dQ reduction.
 //
+// Work items are ordered heaviest first over all heads under the causal
+// mask, and in L2-sized groups of heads without it.  Mask variants (a causal
+// sliding window; documents of packed sequences, see mask.cuh) have their
+// own instantiations: items end at the last query tile that still sees the
+// key/value tile, and the softmax warps zero P outside the mask on the edge
+// tiles; with documents, the preprocessing step tabulates those ranges and a
+// one-CTA sort (attn_bwd_order_kernel) orders the items by size.  Every
+// kernel is launched with programmatic dependent launch: its set-up overlaps
+// the previous kernel, and it waits (griddepcontrol.wait) before reading.
+//
 // The dQ reduction is the costly exchange of this design: every key/value
 // tile adds a 128 x d fp32 partial into each query tile's accumulator.  Done
 // as one red.global per thread and 16 bytes it saturated the load/store path

@@ -22,6 +22,10 @@
 //    the next S of one tile is computed while the other tile's P V runs.
 //  * Causal: a CTA stops at the last key tile its rows can see; tiles on the
 //    diagonal are masked element-wise.  CTAs are launched heaviest first.
+//    Without the mask they run head by head, sharing K and V in L2.
+//  * Mask variants (mask.cuh: a causal sliding window, documents of packed
+//    sequences) have their own instantiations: a CTA starts at the first key
+//    tile its first row can see, and each row masks keys below its bound.
 //  * Every mbarrier wait is bounded (see ptx.cuh); on expiry the kernel
 //    records an error, drains the tensor core and exits normally.
 
