@@ -68,15 +68,41 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments or blank lines (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':  # string literal, copied whole
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).split("\n")]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: a stored ncu traffic figure is only used if
-    the kernels have not changed since it was captured."""
+    """Hash of the CUDA sources, comments excluded: a stored ncu traffic
+    figure is only used if the kernels' code has not changed since it was
+    captured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_backward_pass_attn_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                code = _strip_comments(f.read())
+            h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
