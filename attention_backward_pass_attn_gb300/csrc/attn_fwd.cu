@@ -307,9 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               u[c] = __float_as_uint(-INFINITY);
           }
         }
-        float mx = __uint_as_float(u[0]);
+        float m8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(u[c]));
+        for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(u[e]);
+#pragma unroll
+        for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(u[e]));
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float mt = mx * scale_log2;  // scale > 0, so the max commutes with it
         const float m_new = fmaxf(m, mt);
         // Lazy rescale: move the reference maximum (and rescale l and O by
@@ -321,20 +325,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
         }
         const float mb = (m == -INFINITY) ? 0.f : m;
-        float rowsum = 0.f;
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
 #pragma unroll
           for (int c2 = 0; c2 < 32; ++c2) {
-            const float p0 = ex2(fmaf(__uint_as_float(u[64 * h + 2 * c2]), scale_log2, -mb));
-            const float p1 = ex2(fmaf(__uint_as_float(u[64 * h + 2 * c2 + 1]), scale_log2, -mb));
-            rowsum += p0 + p1;
+            const float x0 = fmaf(__uint_as_float(u[64 * h + 2 * c2]), scale_log2, -mb);
+            const float x1 = fmaf(__uint_as_float(u[64 * h + 2 * c2 + 1]), scale_log2, -mb);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            rs[c2 & 3] += p0 + p1;
             pk[c2] = pack_bf16x2(p0, p1);
           }
           tmem_st32(tS + 32 * h, pk);
         }
-        l += rowsum;
+        l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         // tcgen05.ld/st are warp-collective: if any row of the warp moved its
         // maximum, the whole warp rescales (alpha = 1 leaves the other rows
         // unchanged).  O holds P V of earlier tiles; PV(j-1) has completed.
