@@ -291,6 +291,15 @@ def pin_brute_force(lib):
 # --------------------------------------------------------------------------
 # Independent library cross-check: PyTorch fp64 CPU attention + autograd.
 # --------------------------------------------------------------------------
+def _sdpa_fp64(torch, q, k, v, **kw):
+    """PyTorch's scaled_dot_product_attention on its plain math backend
+    (matmul and softmax composed in the inputs' fp64), not a fused kernel."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+
+    with sdpa_kernel(SDPBackend.MATH):
+        return torch.nn.functional.scaled_dot_product_attention(q, k, v, **kw)
+
+
 def pin_torch_fp64(lib):
     import torch
 
@@ -302,8 +311,7 @@ def pin_torch_fp64(lib):
             out = _fb(lib, q, k, v, do, causal, s)
             tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True)
                           for x in (q, k, v))
-            to = torch.nn.functional.scaled_dot_product_attention(
-                tq, tk, tv, is_causal=causal, scale=s)
+            to = _sdpa_fp64(torch, tq, tk, tv, is_causal=causal, scale=s)
             to.backward(torch.tensor(do, dtype=torch.float64))
             scores = (tq.detach() @ tk.detach().transpose(-1, -2)) * s
             if causal:
@@ -434,8 +442,7 @@ def pin_window_torch_fp64(lib):
         band = (j <= i) & (i - j < W)  # True = attend
         tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True)
                       for x in (q, k, v))
-        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=band,
-                                                              scale=s)
+        to = _sdpa_fp64(torch, tq, tk, tv, attn_mask=band, scale=s)
         to.backward(torch.tensor(do, dtype=torch.float64))
         _close(out["O"], to.detach().numpy(), 1e-11, what="window torch O")
         _close(out["dQ"], tq.grad.numpy(), 1e-10, what="window torch dQ")
@@ -509,8 +516,7 @@ def pin_doc_torch_fp64(lib):
             allowed &= i - j < W
         tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True)
                       for x in (q, k, v))
-        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=allowed,
-                                                              scale=s)
+        to = _sdpa_fp64(torch, tq, tk, tv, attn_mask=allowed, scale=s)
         to.backward(torch.tensor(do, dtype=torch.float64))
         _close(out["O"], to.detach().numpy(), 1e-11, what="doc torch O")
         _close(out["dQ"], tq.grad.numpy(), 1e-10, what="doc torch dQ")
