@@ -101,3 +101,41 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--workload", "b1h2n128d64", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, timeout=300, env=env)
     assert p.returncode == 0 and p.stdout.strip() == ""
+
+
+def _visible_pairs(N, causal, window=0, lengths=()):
+    """Brute-force count of the (query, key) pairs the mask lets through."""
+    doc = []
+    for n in lengths:
+        doc += [len(doc)] * n
+    count = 0
+    for i in range(N):
+        for j in range(N):
+            if causal and j > i:
+                continue
+            if window and i - j >= window:
+                continue
+            if lengths and doc[j] < doc[i]:
+                continue
+            count += 1
+    return count
+
+
+@pytest.mark.parametrize("N,causal,window,lengths", [
+    (37, False, 0, ()), (37, True, 0, ()), (64, True, 9, ()), (64, True, 64, ()),
+    (50, True, 0, (20, 1, 29)), (128, True, 0, (128,))])
+def test_flop_pairs_follow_the_mask(N, causal, window, lengths):
+    """The FLOP accounting counts the area of the visible region: the brute-force
+    pair count minus half of its diagonal band (N^2/2 under the causal mask, the
+    usual convention), so both arms are measured against the same work."""
+    from attention_backward_pass_attn_gb300.inputs import Workload
+
+    w = Workload("t", 1, 1, N, 64, causal, seed=0, window=window, doc_lengths=lengths)
+    exact = _visible_pairs(N, causal, window, lengths)
+    if not causal:
+        assert w.pairs() == exact
+    elif 0 < window < N:
+        assert w.pairs() == exact - window / 2
+    else:
+        assert w.pairs() == exact - N / 2
+    assert w.bwd_flops() == 10 * 64 * w.pairs() and w.fwd_flops() == 4 * 64 * w.pairs()
