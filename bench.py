@@ -21,9 +21,11 @@ Legs reported on the one JSON line (rank 0):
               run on their own streams and overlap neighbouring steps
   roofline    the backward main kernel (tensor-bound) against the measured
               dense bf16 peak
-  cpu_baseline the fp64 oracle on the host cores, on a bounded sample
+  cpu_baseline the fp64 oracle on the host cores (their count and CPU model),
+              on a bounded sample
   d128_backward  the three d = 128 workloads (N >= 4096), main-kernel TF/s,
-              and sliding-window attention (N = 16384, a 4096-key window)
+              sliding-window attention (N = 16384, a 4096-key window) and
+              packed documents (N = 16384, six documents)
 
 --impl reference times the fp64 CPU oracle (the only reference this project
 has) on the same workload, metric and unit.
@@ -40,6 +42,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -342,6 +345,25 @@ def e2e_workload(w, steps: int, warmup: int):
     return ms, h2d, d2h, resident
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo, else lscpu), or the machine type."""
+    try:
+        with open("/proc/cpuinfo", encoding="utf-8") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(w, min_seconds: float = 10.0):
     """The fp64 oracle, as it stands, on the host cores: whole passes over the
     workload's heads until at least `min_seconds` of CPU wall time."""
@@ -359,7 +381,7 @@ def cpu_baseline(w, min_seconds: float = 10.0):
             break
     per_pass = el / passes
     return {"value": w.bwd_flops() / per_pass / 1e12, "unit": "TFLOP/s",
-            "cores": oracle.max_threads(lib), "kind": "oracle",
+            "cores": oracle.max_threads(lib), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": "%d full pass(es) of %s (all %d heads), fp64 fwd+bwd, %.1f s each; "
                       "backward FLOPs / pass time" % (passes, w.name, w.heads, per_pass)}
 
@@ -579,8 +601,8 @@ def run_reference(args):
         "data": "synthetic: seeded N(0,1) bf16 inputs (no dataset)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                    "causal": w.causal},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -92,6 +92,7 @@ def test_reference_arm_runs_on_cpu():
     line = json.loads(p.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
