@@ -11,8 +11,9 @@ from .inputs import WORKLOADS, WORKLOAD_ORDER, Workload, make_inputs  # noqa: F4
 
 _BINDING_NAMES = (
     "attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
-    "attn_bwd_dq_convert", "attn_bwd_workspace_size", "attn_last_device_error",
-    "AttnError", "load_library",
+    "attn_bwd_dq_convert", "attn_bwd_workspace_size", "alloc_workspace",
+    "attn_last_device_error", "attn_device_error_word", "attn_watchdog_selftest",
+    "status_string", "AttnError", "load_library",
 )
 
 
