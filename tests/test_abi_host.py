@@ -156,3 +156,9 @@ def test_binding_checks_tensors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         ab.attn_fwd(q, q, q, causal=False)  # CPU tensors are rejected, nothing falls back
+
+
+def test_missing_library_raises(tmp_path):
+    """Without the built CUDA library the binding raises; there is no other path."""
+    with pytest.raises(RuntimeError, match="not built"):
+        ab.load_library(str(tmp_path / "libattn_gb300.so"))
