@@ -95,6 +95,7 @@ int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, 
                 void* stream);
 
 /*
+ * Interface utility of this library's boundary; the paper has no counterpart.
  * Bytes of device workspace attn_bwd needs for this shape (0 for an empty
  * problem).  Holds, per head, D = rowsum(dO o O) and L scaled to base 2, each
  * [roundup(N,128)] fp32, an fp32 dQ accumulator of roundup(N,128) x d,
@@ -168,13 +169,18 @@ int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const
  * up the scratch's device address; make it before any stream capture on that
  * device.  All calls share the scratch (it keeps the last call's contents,
  * and every call rewrites what it reads), so calls that overlap on the GPU,
- * e.g. on two streams, race: order them on one stream.
+ * e.g. on two streams, race: order them on one stream.  The address is
+ * looked up once per device and kept for the life of the process, so a
+ * cudaDeviceReset after the first call on a device is not supported (the
+ * same holds for the error word every entry point reports into).
  */
 int attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
                      int causal, float scale, void* stream);
 
 /*
+ * Interface utility of this library's boundary (failure detection); the paper
+ * has no counterpart.
  * Synchronise `stream`, then read and clear the current device's error word.
  * Returns ATTN_OK if no kernel reported a failure since the last call,
  * ATTN_ERR_TIMEOUT if a bounded wait ran out, ATTN_ERR_DEVICE for another
@@ -183,12 +189,14 @@ int attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
 int attn_last_device_error(void* stream);
 
 /*
+ * Interface utility; the paper has no counterpart.
  * Like attn_last_device_error, but also stores the raw error word
  * ((code << 24) | site, 0 if none) in *word before clearing it.
  */
 int attn_device_error_word(void* stream, int* word);
 
 /*
+ * Interface utility; the paper has no counterpart.
  * Failure-detection self-test: launches one tiny kernel whose bounded
  * mbarrier wait can never be satisfied (nothing arrives), with a limit of
  * `limit_ns` nanoseconds (1e3 .. 1e10).  The kernel gives up, records
@@ -197,10 +205,12 @@ int attn_device_error_word(void* stream, int* word);
  */
 int attn_watchdog_selftest(uint64_t limit_ns, void* stream);
 
-/* Static text for a status code. */
+/* Interface utility; the paper has no counterpart.  Static text for a status
+ * code. */
 const char* attn_status_string(int status);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Interface utility; the paper has no counterpart.  Library version,
+ * major * 10000 + minor * 100 + patch. */
 int attn_version(void);
 
 #ifdef __cplusplus

@@ -329,26 +329,34 @@ def pin_torch_fp64(lib):
 
 def pin_row_sampler_matches_full(lib):
     """The row sampler evaluates the same definition as the full oracle: its
-    rows equal the full result's rows bit for bit (same arithmetic order)."""
+    rows equal the full result's rows bit for bit (same arithmetic order),
+    under every mask it takes -- none, causal, a sliding window, documents,
+    and documents with a window.  The large-size GPU tests of the mask
+    variants rely on the sampler in those modes."""
     rng = np.random.default_rng(19)
-    for causal in (False, True):
-        N, d = 57, 6
+    N, d = 57, 6
+    docs = doc_map([9, 1, 20, 27])  # a one-position document, documents across the rows
+    cases = [(False, 0, None), (True, 0, None), (True, 5, None), (True, 1, None),
+             (True, 0, docs), (True, 7, docs)]
+    for causal, window, doc in cases:
         q, k, v, do = (_rand(rng, (1, 1, N, d)) for _ in range(4))
-        full = _fb(lib, q, k, v, do, causal, 0.35)
-        qr, kr = [0, 5, 56, 31], [56, 0, 13]
+        full = _fb(lib, q, k, v, do, causal, 0.35, window=window,
+                   doc=None if doc is None else doc[None, :])
+        qr, kr = [0, 5, 9, 10, 56, 31], [56, 0, 9, 13, 30]
+        what = "causal=%s window=%d doc=%s" % (causal, window, doc is not None)
         rows = oracle.attention_head_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, 0.35,
-                                          qr, kr, lib=lib)
+                                          qr, kr, lib=lib, window=window, doc=doc)
         for name in ("O", "dQ"):
-            assert np.array_equal(rows[name], full[name][0, 0][qr]), name
-        assert np.array_equal(rows["L"], full["L"][0, 0][qr])
+            assert np.array_equal(rows[name], full[name][0, 0][qr]), (name, what)
+        assert np.array_equal(rows["L"], full["L"][0, 0][qr]), what
         for name in ("dK", "dV"):
-            assert np.array_equal(rows[name], full[name][0, 0][kr]), name
+            assert np.array_equal(rows[name], full[name][0, 0][kr]), (name, what)
         # query rows only (no key rows): each row is evaluated on its own
         qonly = oracle.attention_head_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, 0.35,
-                                           qr, [], lib=lib)
+                                           qr, [], lib=lib, window=window, doc=doc)
         for name in ("O", "dQ"):
-            assert np.array_equal(qonly[name], full[name][0, 0][qr]), name
-        assert np.array_equal(qonly["L"], full["L"][0, 0][qr])
+            assert np.array_equal(qonly[name], full[name][0, 0][qr]), (name, what)
+        assert np.array_equal(qonly["L"], full["L"][0, 0][qr]), what
 
 
 # --------------------------------------------------------------------------

@@ -127,6 +127,26 @@ def test_bwd_validation(lib):
     assert lib.attn_watchdog_selftest(10, None) == ab.ATTN_ERR_INVALID_ARG
 
 
+def test_noalloc_passes_argument_errors_through(lib):
+    """attn_bwd_noalloc answers every bad argument the way attn_bwd does, before
+    it looks up its scratch (nothing here reaches the GPU): an unsupported head
+    dim, a null or misaligned pointer, a bad scale, and an empty problem, which
+    is valid and launches nothing."""
+    def noalloc(ptr=FAKE, B=1, H=1, N=128, d=64, causal=0, scale=0.125, q=None):
+        qp = ptr if q is None else q
+        return lib.attn_bwd_noalloc(qp, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, B, H, N, d,
+                                    causal, scale, None)
+    assert noalloc(d=96) == ab.ATTN_ERR_UNSUPPORTED
+    assert noalloc(ptr=None) == ab.ATTN_ERR_INVALID_ARG
+    assert noalloc(q=FAKE + 8) == ab.ATTN_ERR_INVALID_ARG   # misaligned Q
+    assert noalloc(q=0) == ab.ATTN_ERR_INVALID_ARG          # null Q only
+    assert noalloc(scale=0.0) == ab.ATTN_ERR_INVALID_ARG
+    assert noalloc(causal=3) == ab.ATTN_ERR_INVALID_ARG
+    assert noalloc(B=-1) == ab.ATTN_ERR_INVALID_ARG
+    assert noalloc(ptr=None, B=0) == ab.ATTN_OK
+    assert noalloc(ptr=None, N=0) == ab.ATTN_OK
+
+
 def test_window_validation(lib):
     """The sliding window is causal only and non-negative; checked before
     anything else is looked at, empty problems included."""

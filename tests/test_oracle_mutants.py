@@ -29,6 +29,10 @@ MUTANTS = {
     "doc_start_one_early": ("if (mk->causal && mk->doc && mk->doc[i] > lo) lo = mk->doc[i];",
                             "if (mk->causal && mk->doc && mk->doc[i] - 1 > lo) lo = mk->doc[i] - 1;"),
     "dkdv_ignores_documents": ("if (row_start(i, mk) > j) continue;", ""),
+    "sampler_ignores_documents": ("const Mask mk = {causal, window, doc};",
+                                  "const Mask mk = {causal, window, NULL};"),
+    "sampler_ignores_window": ("const Mask mk = {causal, window, doc};",
+                               "const Mask mk = {causal, 0, doc};"),
     "D_uses_wrong_row": ("if (dOh && Di_out) *Di_out = dot(dOh + i * d, Oi, d);",
                          "if (dOh && Di_out) *Di_out = dot(dOh + (N - 1 - i) * d, Oi, d);"),
 }
