@@ -224,6 +224,18 @@ def barrier():
         dist.barrier()
 
 
+def workload_of(args):
+    """The named workload, or (with --batch B) the same shape with B batch
+    elements, renamed after its shape."""
+    from attention_backward_pass_attn_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    if args.batch > 0 and args.batch != w.B:
+        name = "b%dh%dn%dd%d%s" % (args.batch, w.H, w.N, w.d, "_causal" if w.causal else "")
+        w = w.with_shape(B=args.batch, name=name)
+    return w
+
+
 def config_dict(w) -> dict:
     """The `config` object of the JSON line, the same for both arms."""
     return {
@@ -433,7 +445,7 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks["bf16_tflops"])
     peak_sus = float(peaks.get("bf16_tflops_sustained", peak_tf))
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     dev = torch.device("cuda", torch.cuda.current_device())
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -583,7 +595,7 @@ def run_reference(args):
     import oracle
     from attention_backward_pass_attn_gb300.inputs import WORKLOADS, make_inputs
 
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     q, k, v, do = make_inputs(w)
     flat = [t.reshape(w.B * w.H, 1, w.N, w.d) for t in (q, k, v, do)]
     lib = oracle.load()
@@ -640,6 +652,9 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=HEADLINE)
+    p.add_argument("--batch", type=int, default=0,
+                   help="run the workload with this many batch elements instead (a smaller "
+                        "case of the same kernels, for profiler captures); 0 = as named")
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args(argv)
