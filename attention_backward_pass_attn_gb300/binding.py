@@ -27,6 +27,11 @@ ATTN_ERR_WORKSPACE = 5
 ATTN_ERR_DEVICE = 6
 ATTN_ERR_TOO_LARGE = 7
 
+# How attn_bwd forms dQ (attn_dq_method_t in include/attn.h).
+ATTN_DQ_AUTO = 0
+ATTN_DQ_REDUCE = 1
+ATTN_DQ_SEPARATE = 2
+
 _lock = threading.Lock()
 _lib = None
 
@@ -59,6 +64,10 @@ def load_library(path: str | None = None):
             "attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp,
                                 sz, vp]),
+            "attn_bwd_opts": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f,
+                                  i, vp, sz, vp]),
+            "attn_bwd_main_dkdv": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
+            "attn_bwd_dq": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_preprocess": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
             "attn_bwd_main": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_dq_convert": (i, [vp, i, i, i, i, f, vp, sz, vp]),
@@ -163,10 +172,13 @@ def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None,
 
 
 def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None, window=0, doc=None):
-    """dQ, dK, dV of exact attention (the fused backward, three kernels).
+             workspace=None, stream=None, window=0, doc=None, dq_method=ATTN_DQ_AUTO):
+    """dQ, dK, dV of exact attention (the fused backward).
 
     o, lse: the forward's outputs; do: the upstream gradient of o.
+    dq_method: ATTN_DQ_AUTO, ATTN_DQ_REDUCE (the main kernel reduces dQ
+    partials into an fp32 accumulator) or ATTN_DQ_SEPARATE (a separate
+    query-stationary dQ pass).
     Returns (dQ, dK, dV), bf16 [B, H, N, d].
     """
     B, H, N, d = _shape4(q, "q")
@@ -180,14 +192,15 @@ def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv
         _check_tensor(t, n, (B, H, N, d))
     if workspace is None:
         workspace = alloc_workspace(B, H, N, d, q.device)
-    st = load_library().attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                    do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                    dv.data_ptr(), B, H, N, d, int(bool(causal)), int(window),
-                                    _doc_ptr(doc, B, N), _default_scale(d, scale),
-                                    workspace.data_ptr(),
-                                    workspace.numel() * workspace.element_size(),
-                                    _stream(stream))
-    _check("attn_bwd_ex", st)
+    st = load_library().attn_bwd_opts(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                      dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                      int(bool(causal)), int(window), _doc_ptr(doc, B, N),
+                                      _default_scale(d, scale), int(dq_method),
+                                      workspace.data_ptr(),
+                                      workspace.numel() * workspace.element_size(),
+                                      _stream(stream))
+    _check("attn_bwd_opts", st)
     return dq, dk, dv
 
 
@@ -209,6 +222,27 @@ def attn_bwd_main(q, k, v, do, dk, dv, causal: bool, workspace, scale=None, stre
                                       workspace.numel() * workspace.element_size(),
                                       _stream(stream))
     _check("attn_bwd_main", st)
+
+
+def attn_bwd_main_dkdv(q, k, v, do, dk, dv, causal: bool, workspace, scale=None, stream=None):
+    B, H, N, d = _shape4(q, "q")
+    st = load_library().attn_bwd_main_dkdv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                           do.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N,
+                                           d, int(bool(causal)), _default_scale(d, scale),
+                                           workspace.data_ptr(),
+                                           workspace.numel() * workspace.element_size(),
+                                           _stream(stream))
+    _check("attn_bwd_main_dkdv", st)
+
+
+def attn_bwd_dq(q, k, v, do, dq, causal: bool, workspace, scale=None, stream=None):
+    B, H, N, d = _shape4(q, "q")
+    st = load_library().attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                    dq.data_ptr(), B, H, N, d, int(bool(causal)),
+                                    _default_scale(d, scale), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check("attn_bwd_dq", st)
 
 
 def attn_bwd_dq_convert(dq, workspace, scale=None, stream=None):

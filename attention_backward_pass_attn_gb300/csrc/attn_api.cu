@@ -162,20 +162,46 @@ int make_acc_map(CUtensorMap* map, const float* acc, const Shape& s) {
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
-// The main kernel for a validated, non-empty shape (mask included).
+// The main kernel for a validated, non-empty shape (mask included): with
+// `fused_dq` the instantiation that also adds dQ partials into the
+// workspace's accumulator, else the one that forms dK and dV only.
 int bwd_main_launch(const void* Q, const void* K, const void* V, const void* dO, void* dK,
-                    void* dV, const Shape& s, float scale, void* workspace, void* stream) {
+                    void* dV, const Shape& s, float scale, void* workspace, bool fused_dq,
+                    void* stream) {
   int* err = error_word_ptr();
   if (!err) return ATTN_ERR_CUDA;
   const Workspace ws = carve_workspace(workspace, s);
   CUtensorMap mq, mk, mv, mdo, macc;
   if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s) ||
-      make_tile_map(&mdo, dO, s) || make_acc_map(&macc, ws.acc, s))
+      make_tile_map(&mdo, dO, s))
     return ATTN_ERR_CUDA;
+  if (!fused_dq)
+    return cuda_status(
+        launch_bwd_main_dkdv(mq, mk, mv, mdo, dK, dV, ws, s, scale, err, (cudaStream_t)stream));
+  if (make_acc_map(&macc, ws.acc, s)) return ATTN_ERR_CUDA;
   return cuda_status(launch_bwd_main(mq, mk, mv, mdo, macc, dK, dV, ws, s, scale, err,
                                      (cudaStream_t)stream));
 }
 
+// The separate dQ pass for a validated, non-empty shape (mask included).
+int bwd_dq_launch(const void* Q, const void* K, const void* V, const void* dO, void* dQ,
+                  const Shape& s, float scale, void* workspace, void* stream) {
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo;
+  if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s) ||
+      make_tile_map(&mdo, dO, s))
+    return ATTN_ERR_CUDA;
+  return cuda_status(launch_bwd_dq(mq, mk, mv, mdo, dQ, carve_workspace(workspace, s), s, scale,
+                                   err, (cudaStream_t)stream));
+}
+
+// The dQ method attn_bwd uses when the caller leaves the choice to the
+// library.
+int auto_dq_method(const Shape& s) {
+  (void)s;
+  return ATTN_DQ_REDUCE;
+}
 
 }  // namespace attn
 
@@ -240,7 +266,7 @@ int attn_bwd_preprocess(const void* O, const void* dO, const float* L, int B, in
   if (empty) return ATTN_OK;
   if ((st = check_ptrs({O, dO, L})) != ATTN_OK) return st;
   if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
-  return cuda_status(launch_bwd_preprocess(O, dO, L, carve_workspace(workspace, s), s,
+  return cuda_status(launch_bwd_preprocess(O, dO, L, carve_workspace(workspace, s), s, true,
                                            (cudaStream_t)stream));
 }
 
@@ -255,7 +281,35 @@ int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, v
   if (empty) return ATTN_OK;
   if ((st = check_ptrs({Q, K, V, dO, dK, dV})) != ATTN_OK) return st;
   if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
-  return bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, stream);
+  return bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, true, stream);
+}
+
+int attn_bwd_main_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                       void* dV, int B, int H, int N, int d, int causal, float scale,
+                       void* workspace, size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q, K, V, dO, dK, dV})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  return bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, false, stream);
+}
+
+int attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
+                int H, int N, int d, int causal, float scale, const void* workspace,
+                size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q, K, V, dO, dQ})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  return bwd_dq_launch(Q, K, V, dO, dQ, s, scale, const_cast<void*>(workspace), stream);
 }
 
 int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
@@ -283,24 +337,36 @@ int attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, cons
                 const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
                 int causal, int window, const int* doc_start, float scale, void* workspace,
                 size_t workspace_bytes_, void* stream) {
+  return attn_bwd_opts(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, causal, window, doc_start,
+                       scale, ATTN_DQ_AUTO, workspace, workspace_bytes_, stream);
+}
+
+int attn_bwd_opts(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                  const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                  int causal, int window, const int* doc_start, float scale, int dq_method,
+                  void* workspace, size_t workspace_bytes_, void* stream) {
   Shape s;
   bool empty = false;
   int st = make_shape(B, H, N, d, causal, &s, &empty);
   if (st != ATTN_OK) return st;
   if ((st = check_mask(causal, window, doc_start)) != ATTN_OK) return st;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dq_method != ATTN_DQ_AUTO && dq_method != ATTN_DQ_REDUCE && dq_method != ATTN_DQ_SEPARATE)
+    return ATTN_ERR_INVALID_ARG;
   if (empty) return ATTN_OK;
   set_mask(&s, window, doc_start);
   if ((st = check_ptrs({Q, K, V, O, dO, L, dQ, dK, dV})) != ATTN_OK) return st;
   if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  const bool fused = (dq_method == ATTN_DQ_AUTO ? auto_dq_method(s) : dq_method) == ATTN_DQ_REDUCE;
   const Workspace ws = carve_workspace(workspace, s);
-  if ((st = cuda_status(launch_bwd_preprocess(O, dO, L, ws, s, (cudaStream_t)stream))) !=
+  if ((st = cuda_status(launch_bwd_preprocess(O, dO, L, ws, s, fused, (cudaStream_t)stream))) !=
       ATTN_OK)
     return st;
   if (s.doc && (st = cuda_status(launch_bwd_order(ws, s, (cudaStream_t)stream))) != ATTN_OK)
     return st;
-  if ((st = bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, stream)) != ATTN_OK)
+  if ((st = bwd_main_launch(Q, K, V, dO, dK, dV, s, scale, workspace, fused, stream)) != ATTN_OK)
     return st;
+  if (!fused) return bwd_dq_launch(Q, K, V, dO, dQ, s, scale, workspace, stream);
   return cuda_status(launch_bwd_dq_convert(dQ, ws, s, scale, (cudaStream_t)stream));
 }
 

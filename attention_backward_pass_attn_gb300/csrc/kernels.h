@@ -100,13 +100,31 @@ cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
                        void* O, float* L, const Shape& s, float scale, int* err,
                        cudaStream_t stream);
 
+// D, L log2(e) (and the document tables); zeroes the dQ accumulator only if
+// zero_acc (the fused main kernel reduces into it; the separate dQ pass does
+// not use it).
 cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
-                                  const Workspace& ws, const Shape& s, cudaStream_t stream);
+                                  const Workspace& ws, const Shape& s, bool zero_acc,
+                                  cudaStream_t stream);
 
 cudaError_t launch_bwd_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO,
                             const CUtensorMap& tmAcc, void* dK, void* dV, const Workspace& ws,
                             const Shape& s, float scale, int* err, cudaStream_t stream);
+
+// The main kernel without the dQ contraction (dK and dV only), for use with
+// the separate dQ pass below.
+cudaError_t launch_bwd_main_dkdv(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmdO, void* dK,
+                                 void* dV, const Workspace& ws, const Shape& s, float scale,
+                                 int* err, cudaStream_t stream);
+
+// The separate query-stationary dQ pass: recomputes S and dP per key/value
+// tile, keeps dQ in tensor memory and writes bf16(scale * dQ).  Needs the
+// preprocessing step's L log2(e) and D (and, with documents, nothing more).
+cudaError_t launch_bwd_dq(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const CUtensorMap& tmdO, void* dQ, const Workspace& ws, const Shape& s,
+                          float scale, int* err, cudaStream_t stream);
 
 // With documents: sorts the work items by their query-tile count (from the
 // preprocessing step's table) so that the main kernel deals them out heaviest

@@ -250,7 +250,7 @@ def config_dict(w) -> dict:
 
 
 # ----------------------------------------------------------------------------- our arm
-def time_workload(w, steps: int, warmup: int, flush, split=False):
+def time_workload(w, steps: int, warmup: int, flush, split=False, dq_method=None):
     """Run fwd + bwd `warmup + steps` times; returns per-step event times (ms).
 
     Events go before the forward, between forward and backward, and after the
@@ -272,20 +272,29 @@ def time_workload(w, steps: int, warmup: int, flush, split=False):
     stream = torch.cuda.current_stream()
     dmap = make_doc_map(w)
     dmap = dmap.to(dev) if dmap is not None else None
+    method = ab.ATTN_DQ_AUTO if dq_method is None else dq_method
 
     def step():
         ab.attn_fwd(q, k, v, w.causal, w.scale, out=o, lse=lse, stream=stream, window=w.window,
                     doc=dmap)
         e[1].record(stream)
-        if split:
+        if split and method == ab.ATTN_DQ_SEPARATE:
+            ab.attn_bwd_preprocess(o, do, lse, ws, stream=stream)
+            e[2].record(stream)
+            ab.attn_bwd_main_dkdv(q, k, v, do, dk, dv, w.causal, ws, scale=w.scale,
+                                  stream=stream)
+            e[3].record(stream)
+            ab.attn_bwd_dq(q, k, v, do, dq, w.causal, ws, scale=w.scale, stream=stream)
+        elif split:
             ab.attn_bwd_preprocess(o, do, lse, ws, stream=stream)
             e[2].record(stream)
             ab.attn_bwd_main(q, k, v, do, dk, dv, w.causal, ws, scale=w.scale, stream=stream)
             e[3].record(stream)
             ab.attn_bwd_dq_convert(dq, ws, scale=w.scale, stream=stream)
-        else:  # the public call: the same three kernels
+        else:  # the public call
             ab.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, dq=dq, dk=dk, dv=dv,
-                        workspace=ws, stream=stream, window=w.window, doc=dmap)
+                        workspace=ws, stream=stream, window=w.window, doc=dmap,
+                        dq_method=method)
 
     rec = []
     for i in range(warmup + steps):
@@ -501,6 +510,26 @@ def run_ours(args):
                 "main_ms_median": round(mm, 4),
                 "bwd_ms_median": round(statistics.median(rw["bwd"]), 4),
             }
+        # The two ways of forming dQ, timed against each other: the main
+        # kernel reducing dQ partials into an fp32 accumulator, or a separate
+        # query-stationary pass (two extra contractions, no accumulator).
+        from attention_backward_pass_attn_gb300.binding import ATTN_DQ_REDUCE, ATTN_DQ_SEPARATE
+        cmp = {}
+        for name in [w.name] + OTHER:
+            cw = w if name == w.name else WORKLOADS[name]
+            red = time_workload(cw, 10, 3, flush, dq_method=ATTN_DQ_REDUCE)
+            sep = time_workload(cw, 10, 3, flush, dq_method=ATTN_DQ_SEPARATE)
+            sep_split = time_workload(cw, 10, 3, flush, split=True, dq_method=ATTN_DQ_SEPARATE)
+            r_ms, s_ms = statistics.median(red["bwd"]), statistics.median(sep["bwd"])
+            cmp[name] = {
+                "reduce_bwd_ms": round(r_ms, 4), "separate_bwd_ms": round(s_ms, 4),
+                "reduce_bwd_tflops": round(cw.bwd_flops() / r_ms / 1e9, 1),
+                "separate_bwd_tflops": round(cw.bwd_flops() / s_ms / 1e9, 1),
+                "separate_main_dkdv_ms": round(statistics.median(sep_split["main"]), 4),
+                "separate_dq_pass_ms": round(statistics.median(sep_split["conv"]), 4),
+                "faster": "reduce" if r_ms <= s_ms else "separate",
+            }
+        extra["dq_methods"] = cmp
         # Mask variants: a sliding window (4096 keys) and packed documents.
         # FLOPs are those of the visible pairs: N*W - W^2/2 per head under the
         # window, the sum of n^2/2 over documents of lengths n.

@@ -130,6 +130,37 @@ int attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, cons
                 size_t workspace_bytes, void* stream);
 
 /*
+ * How the backward forms dQ_i = s sum_j dS_ij k_j, a sum over key tiles while
+ * the main kernel walks key tiles (the backward of the page section "Flash
+ * Attention"):
+ *
+ *   ATTN_DQ_REDUCE    the main kernel also forms each key tile's partial
+ *                     dS K and adds it into an fp32 accumulator in the
+ *                     workspace (TMA reduce-add); a last kernel converts it
+ *                     to bf16.  Five contractions per tile pair.  The fp32
+ *                     summation order varies between runs (dQ repeats to
+ *                     about 1e-3 relative; dK, dV bitwise).
+ *   ATTN_DQ_SEPARATE  the main kernel forms dK and dV only; a separate
+ *                     query-stationary pass recomputes S and dP per key tile
+ *                     (the activation recomputation of section "Harnessing
+ *                     the MI300 Hardware Specs") and keeps dQ in tensor
+ *                     memory.  Seven contractions per tile pair, no
+ *                     accumulator traffic, every output bitwise repeatable.
+ *   ATTN_DQ_AUTO      the library's choice for the shape (measured on GB300).
+ */
+typedef enum { ATTN_DQ_AUTO = 0, ATTN_DQ_REDUCE = 1, ATTN_DQ_SEPARATE = 2 } attn_dq_method_t;
+
+/*
+ * attn_bwd_ex with the dQ method chosen by the caller (attn_dq_method_t;
+ * another value is ATTN_ERR_INVALID_ARG).  Same workspace, results (within
+ * rounding) and errors as attn_bwd_ex, which is this call with ATTN_DQ_AUTO.
+ */
+int attn_bwd_opts(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                  const float* L, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                  int causal, int window, const int* doc_start, float scale, int dq_method,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Step 1 of attn_bwd: D_i = <dO_i, O_i> in fp32 and L_i * log2(e) into the
  * workspace, and zero the workspace's dQ accumulator.  Bound by HBM
  * bandwidth.
@@ -154,6 +185,28 @@ int attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, v
  */
 int attn_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, const void* workspace,
                         size_t workspace_bytes, void* stream);
+
+/*
+ * Step 2 of the ATTN_DQ_SEPARATE backward: the main kernel without the dQ
+ * contraction -- dV += P^T dO and dK += dS^T Q per key/value tile, written
+ * as bf16 dK, dV.  Requires attn_bwd_preprocess on the same workspace (whose
+ * dQ accumulator it does not use).
+ */
+int attn_bwd_main_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                       void* dV, int B, int H, int N, int d, int causal, float scale,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Step 3 of the ATTN_DQ_SEPARATE backward: the query-stationary dQ pass.  Per
+ * pair of 128-row query tiles it recomputes S = s Q K^T, P = exp(S - L),
+ * dP = dO V^T and dS = P o (dP - D) for every key/value tile the mask lets it
+ * see, accumulates dQ += dS K in tensor memory, and writes dQ (bf16).
+ * Requires attn_bwd_preprocess (L and D) on the same workspace; it does not
+ * depend on step 2, and writes nothing step 2 reads.
+ */
+int attn_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, void* dQ, int B,
+                int H, int N, int d, int causal, float scale, const void* workspace,
+                size_t workspace_bytes, void* stream);
 
 /*
  * Backward without any device allocation, for callers that cannot call

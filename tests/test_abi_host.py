@@ -127,6 +127,32 @@ def test_bwd_validation(lib):
     assert lib.attn_watchdog_selftest(10, None) == ab.ATTN_ERR_INVALID_ARG
 
 
+def test_dq_method_and_split_steps_validation(lib):
+    """attn_bwd_opts takes only the three documented dQ methods; the two steps
+    of the separate-pass backward validate like the other steps."""
+    need = lib.attn_bwd_workspace_size(1, 1, 128, 64)
+
+    def opts(method, N=128, ptr=FAKE):
+        return lib.attn_bwd_opts(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, N, 64, 1, 0,
+                                 None, 0.125, method, FAKE, need, None)
+    for bad in (-1, 3, 99):
+        assert opts(bad) == ab.ATTN_ERR_INVALID_ARG
+        assert opts(bad, N=0, ptr=None) == ab.ATTN_ERR_INVALID_ARG
+    for good in (ab.ATTN_DQ_AUTO, ab.ATTN_DQ_REDUCE, ab.ATTN_DQ_SEPARATE):
+        assert opts(good, N=0, ptr=None) == ab.ATTN_OK
+        assert opts(good, ptr=None) == ab.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_main_dkdv(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 1, 128, 64, 1, 0.125,
+                                  FAKE, need, None) == ab.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_main_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 96, 1, 0.125,
+                                  FAKE, need, None) == ab.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 1, 0.125, FAKE, need - 1,
+                           None) == ab.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE + 8, 1, 1, 128, 64, 1, 0.125, FAKE, need,
+                           None) == ab.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_dq(None, None, None, None, None, 1, 1, 0, 64, 1, 0.125, None, 0,
+                           None) == ab.ATTN_OK
+
+
 def test_noalloc_passes_argument_errors_through(lib):
     """attn_bwd_noalloc answers every bad argument the way attn_bwd does, before
     it looks up its scratch (nothing here reaches the GPU): an unsupported head

@@ -65,12 +65,16 @@ def random_lengths(rng, N, lo, hi):
     return lengths
 
 
-def run(q, k, v, do, scale, window, docs):
+METHODS = {"reduce": ab.ATTN_DQ_REDUCE, "separate": ab.ATTN_DQ_SEPARATE}
+
+
+def run(q, k, v, do, scale, window, docs, dq_method=ab.ATTN_DQ_AUTO):
     dev = torch.device("cuda", 0)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     dmap = torch.from_numpy(docs.astype(np.int32)).to(dev)
     o, lse = ab.attn_fwd(qd, kd, vd, True, scale, window=window, doc=dmap)
-    dq, dk, dv = ab.attn_bwd(qd, kd, vd, o, dod, lse, True, scale, window=window, doc=dmap)
+    dq, dk, dv = ab.attn_bwd(qd, kd, vd, o, dod, lse, True, scale, window=window, doc=dmap,
+                             dq_method=dq_method)
     torch.cuda.synchronize()
     return dict(O=o, L=lse, dQ=dq, dK=dk, dV=dv)
 
@@ -83,12 +87,13 @@ def check(gpu, ref, what):
     assert lerr <= L_ATOL, msg
 
 
+@pytest.mark.parametrize("method", sorted(METHODS))
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N,lo,hi,window", [(129, 1, 40, 0), (300, 20, 200, 0),
                                             (700, 100, 400, 0), (1000, 1, 700, 0),
                                             (640, 128, 128, 0), (900, 50, 500, 96),
                                             (513, 200, 513, 300)])
-def test_documents_full_tensors(N, lo, hi, window, d):
+def test_documents_full_tensors(N, lo, hi, window, d, method):
     rng = np.random.default_rng(N * 31 + lo + hi + window + d)
     B, H = 2, 2
     docs = np.stack([doc_map(random_lengths(rng, N, lo, hi)) for _ in range(B)])
@@ -96,8 +101,8 @@ def test_documents_full_tensors(N, lo, hi, window, d):
     q, k, v, do = (make_tensor((B, H, N, d), seed + 7919 * i) for i in range(4))
     scale = 1.0 / math.sqrt(d)
     ref = oracle.attention_forward_backward(q, k, v, do, True, scale, window=window, doc=docs)
-    gpu = run(q, k, v, do, scale, window, docs)
-    check(gpu, ref, "N=%d docs %d..%d W=%d d=%d" % (N, lo, hi, window, d))
+    gpu = run(q, k, v, do, scale, window, docs, METHODS[method])
+    check(gpu, ref, "N=%d docs %d..%d W=%d d=%d dq=%s" % (N, lo, hi, window, d, method))
 
 
 def test_one_document_is_causal():
@@ -116,14 +121,15 @@ def test_one_document_is_causal():
     assert rel_err(g2[0], f64(g1[0])) <= 2e-3
 
 
-def test_documents_long_sequence_sampled():
+@pytest.mark.parametrize("method", sorted(METHODS))
+def test_documents_long_sequence_sampled(method):
     """N = 16384, d = 128, documents of 300 to 5000 positions: sampled rows."""
     B, H, N, d = 1, 4, 16384, 128
     rng = np.random.default_rng(8)
     docs = doc_map(random_lengths(rng, N, 300, 5000))[None]
     q, k, v, do = (make_tensor((B, H, N, d), 950 + i) for i in range(4))
     scale = 1.0 / math.sqrt(d)
-    gpu = run(q, k, v, do, scale, 0, docs)
+    gpu = run(q, k, v, do, scale, 0, docs, METHODS[method])
     starts = sorted(set(docs[0].tolist()))
     for h in (0, H - 1):
         rows = sorted(set([0, 1, 127, 128, N - 1] + starts[:6] + [max(s - 1, 0) for s in starts[:6]]

@@ -57,11 +57,14 @@ def rel_err(gpu, ref):
     return float(np.max(np.abs(g - ref)) / denom) if denom > 0 else float(np.max(np.abs(g)))
 
 
-def gpu_fwd_bwd(q, k, v, do, causal, scale):
+METHODS = {"reduce": ab.ATTN_DQ_REDUCE, "separate": ab.ATTN_DQ_SEPARATE}
+
+
+def gpu_fwd_bwd(q, k, v, do, causal, scale, dq_method=ab.ATTN_DQ_AUTO):
     dev = torch.device("cuda", 0)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     o, lse = ab.attn_fwd(qd, kd, vd, causal, scale)
-    dq, dk, dv = ab.attn_bwd(qd, kd, vd, o, dod, lse, causal, scale)
+    dq, dk, dv = ab.attn_bwd(qd, kd, vd, o, dod, lse, causal, scale, dq_method=dq_method)
     torch.cuda.synchronize()
     return dict(O=o, L=lse, dQ=dq, dK=dk, dV=dv)
 
@@ -77,12 +80,15 @@ def check_full(gpu, ref, what):
 
 @pytest.mark.parametrize("name", ["b1h2n128d64", "b2h16n2048d64_causal"])
 def test_workload_full_tensors(name):
+    """Both ways of forming dQ (reduce-add into an accumulator; the separate
+    query-stationary pass) against the same oracle result."""
     w = WORKLOADS[name]
     q, k, v, do = make_inputs(w)
     ref = oracle.attention_forward_backward(q, k, v, do, w.causal, w.scale)
-    gpu = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale)
-    check_full(gpu, ref, name)
-    assert ab.attn_last_device_error() == ab.ATTN_OK
+    for mname, method in METHODS.items():
+        gpu = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale, method)
+        check_full(gpu, ref, "%s dq=%s" % (name, mname))
+        assert ab.attn_last_device_error() == ab.ATTN_OK
 
 
 @pytest.mark.parametrize("name", ["b1h2n128d64", "b2h16n2048d64_causal"])
@@ -112,18 +118,24 @@ def test_workload_full_size_full_tensors(name):
     140 s and 70 s for these on 16 host cores."""
     w = WORKLOADS[name]
     q, k, v, do = make_inputs(w)
-    gpu = {n: t.cpu() for n, t in gpu_fwd_bwd(q, k, v, do, w.causal, w.scale).items()}
-    assert ab.attn_last_device_error() == ab.ATTN_OK
+    runs = {}
+    for mname, method in METHODS.items():
+        runs[mname] = {n: t.cpu() for n, t in
+                       gpu_fwd_bwd(q, k, v, do, w.causal, w.scale, method).items()}
+        assert ab.attn_last_device_error() == ab.ATTN_OK
+        torch.cuda.empty_cache()
     ref = oracle.attention_forward_backward(q, k, v, do, w.causal, w.scale)
-    errs = check_full(gpu, ref, name)
-    # per-head worst error, so a failure names the head
-    for hname in ("dQ", "dK", "dV"):
-        g = f64(gpu[hname]).reshape(w.heads, -1)
-        r = ref[hname].reshape(w.heads, -1)
-        worst = np.max(np.abs(g - r), axis=1) / np.max(np.abs(r))
-        assert np.all(worst <= TOL), "%s %s: worst head %d (%.2e)" % (
-            name, hname, int(np.argmax(worst)), float(np.max(worst)))
-    assert max(errs.values()) <= TOL
+    for mname, gpu in runs.items():
+        what = "%s dq=%s" % (name, mname)
+        errs = check_full(gpu, ref, what)
+        # per-head worst error, so a failure names the head
+        for hname in ("dQ", "dK", "dV"):
+            g = f64(gpu[hname]).reshape(w.heads, -1)
+            r = ref[hname].reshape(w.heads, -1)
+            worst = np.max(np.abs(g - r), axis=1) / np.max(np.abs(r))
+            assert np.all(worst <= TOL), "%s %s: worst head %d (%.2e)" % (
+                what, hname, int(np.argmax(worst)), float(np.max(worst)))
+        assert max(errs.values()) <= TOL
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
@@ -135,8 +147,9 @@ def test_ragged_lengths(N, d, causal):
     q, k, v, do = (make_tensor((B, H, N, d), seed + 7919 * i) for i in range(4))
     scale = 1.0 / math.sqrt(d)
     ref = oracle.attention_forward_backward(q, k, v, do, causal, scale)
-    gpu = gpu_fwd_bwd(q, k, v, do, causal, scale)
-    check_full(gpu, ref, "N=%d d=%d causal=%s" % (N, d, causal))
+    for mname, method in METHODS.items():
+        gpu = gpu_fwd_bwd(q, k, v, do, causal, scale, method)
+        check_full(gpu, ref, "N=%d d=%d causal=%s dq=%s" % (N, d, causal, mname))
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -147,8 +160,9 @@ def test_zero_queries_uniform_softmax(d):
     q = torch.zeros_like(k)
     for causal in (False, True):
         ref = oracle.attention_forward_backward(q, k, v, do, causal, 1 / math.sqrt(d))
-        gpu = gpu_fwd_bwd(q, k, v, do, causal, 1 / math.sqrt(d))
-        check_full(gpu, ref, "Q=0 d=%d causal=%s" % (d, causal))
+        for mname, method in METHODS.items():
+            gpu = gpu_fwd_bwd(q, k, v, do, causal, 1 / math.sqrt(d), method)
+            check_full(gpu, ref, "Q=0 d=%d causal=%s dq=%s" % (d, causal, mname))
 
 
 @pytest.mark.parametrize("qscale", [4.0, 8.0])
@@ -159,8 +173,9 @@ def test_sharp_softmax(qscale):
     k, v, do = (make_tensor((B, H, N, d), 42 + i) for i in range(3))
     for causal in (False, True):
         ref = oracle.attention_forward_backward(q, k, v, do, causal, 1 / math.sqrt(d))
-        gpu = gpu_fwd_bwd(q, k, v, do, causal, 1 / math.sqrt(d))
-        check_full(gpu, ref, "sharp %g causal=%s" % (qscale, causal))
+        for mname, method in METHODS.items():
+            gpu = gpu_fwd_bwd(q, k, v, do, causal, 1 / math.sqrt(d), method)
+            check_full(gpu, ref, "sharp %g causal=%s dq=%s" % (qscale, causal, mname))
 
 
 def test_non_default_scale():
@@ -168,8 +183,9 @@ def test_non_default_scale():
     q, k, v, do = (make_tensor((B, H, N, d), 51 + i) for i in range(4))
     for scale in (0.02, 0.5):
         ref = oracle.attention_forward_backward(q, k, v, do, True, scale)
-        gpu = gpu_fwd_bwd(q, k, v, do, True, scale)
-        check_full(gpu, ref, "scale %g" % scale)
+        for mname, method in METHODS.items():
+            gpu = gpu_fwd_bwd(q, k, v, do, True, scale, method)
+            check_full(gpu, ref, "scale %g dq=%s" % (scale, mname))
 
 
 def test_empty_problem():
@@ -198,6 +214,31 @@ def test_steps_match_one_call_and_determinism():
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
     # dQ is summed with fp32 atomics across CTAs: equal up to summation order.
     assert rel_err(dq2, f64(dq1)) <= 2e-3
+
+
+def test_separate_dq_steps_and_determinism():
+    """The separate-pass backward equals its three steps run one by one, and
+    every output, dQ included, is bitwise repeatable (no cross-CTA sums)."""
+    w = WORKLOADS["b2h16n2048d64_causal"]
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    o, lse = ab.attn_fwd(q, k, v, True)
+    sep = ab.ATTN_DQ_SEPARATE
+    dq1, dk1, dv1 = ab.attn_bwd(q, k, v, o, do, lse, True, dq_method=sep)
+    dq2, dk2, dv2 = ab.attn_bwd(q, k, v, o, do, lse, True, dq_method=sep)
+    ws = ab.alloc_workspace(w.B, w.H, w.N, w.d, dev)
+    dq3, dk3, dv3 = (torch.empty_like(q) for _ in range(3))
+    ab.attn_bwd_preprocess(o, do, lse, ws)
+    ab.attn_bwd_main_dkdv(q, k, v, do, dk3, dv3, True, ws)
+    ab.attn_bwd_dq(q, k, v, do, dq3, True, ws)
+    dq4, dk4, dv4 = ab.attn_bwd(q, k, v, o, do, lse, True, dq_method=ab.ATTN_DQ_REDUCE)
+    torch.cuda.synchronize()
+    for a, b_, c in ((dq1, dq2, dq3), (dk1, dk2, dk3), (dv1, dv2, dv3)):
+        assert torch.equal(a, b_) and torch.equal(a, c)
+    # dK, dV come from the same arithmetic in both main-kernel families
+    assert torch.equal(dk1, dk4) and torch.equal(dv1, dv4)
+    # dQ: one bf16 rounding of a different fp32 summation order
+    assert rel_err(dq1, f64(dq4)) <= 2e-3
 
 
 def test_watchdog_reports_timeout_without_fault():

@@ -50,28 +50,33 @@ def rel_err(gpu, ref):
     return float(np.max(np.abs(g - ref)) / denom) if denom > 0 else float(np.max(np.abs(g)))
 
 
-def gpu_fwd_bwd(q, k, v, do, scale, window):
+METHODS = {"reduce": ab.ATTN_DQ_REDUCE, "separate": ab.ATTN_DQ_SEPARATE}
+
+
+def gpu_fwd_bwd(q, k, v, do, scale, window, dq_method=ab.ATTN_DQ_AUTO):
     dev = torch.device("cuda", 0)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     o, lse = ab.attn_fwd(qd, kd, vd, True, scale, window=window)
-    dq, dk, dv = ab.attn_bwd(qd, kd, vd, o, dod, lse, True, scale, window=window)
+    dq, dk, dv = ab.attn_bwd(qd, kd, vd, o, dod, lse, True, scale, window=window,
+                             dq_method=dq_method)
     torch.cuda.synchronize()
     return dict(O=o, L=lse, dQ=dq, dK=dk, dV=dv)
 
 
+@pytest.mark.parametrize("method", sorted(METHODS))
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N,window", [(1, 1), (100, 1), (129, 64), (300, 128), (300, 129),
                                       (513, 200), (640, 256), (700, 511), (384, 383)])
-def test_window_full_tensors(N, window, d):
+def test_window_full_tensors(N, window, d, method):
     B, H = 1, 3
     seed = 5000 + N * 8 + window + d
     q, k, v, do = (make_tensor((B, H, N, d), seed + 7919 * i) for i in range(4))
     scale = 1.0 / math.sqrt(d)
     ref = oracle.attention_forward_backward(q, k, v, do, True, scale, window=window)
-    gpu = gpu_fwd_bwd(q, k, v, do, scale, window)
+    gpu = gpu_fwd_bwd(q, k, v, do, scale, window, METHODS[method])
     errs = {n: rel_err(gpu[n], ref[n]) for n in ("O", "dQ", "dK", "dV")}
     lerr = float(np.max(np.abs(f64(gpu["L"]) - ref["L"])))
-    msg = "N=%d W=%d d=%d: %s L %.2e" % (N, window, d, errs, lerr)
+    msg = "N=%d W=%d d=%d dq=%s: %s L %.2e" % (N, window, d, method, errs, lerr)
     assert all(e <= TOL for e in errs.values()), msg
     assert lerr <= L_ATOL, msg
 
@@ -95,12 +100,13 @@ def test_window_at_least_n_is_causal():
     assert rel_err(g2[0], f64(g1[0])) <= 2e-3  # dQ: fp32 reductions, order may differ
 
 
-def test_window_long_sequence_sampled():
+@pytest.mark.parametrize("method", sorted(METHODS))
+def test_window_long_sequence_sampled(method):
     """N = 16384, d = 128, a 4096-key window: sampled rows of two heads."""
     B, H, N, d, W = 1, 4, 16384, 128, 4096
     q, k, v, do = (make_tensor((B, H, N, d), 900 + i) for i in range(4))
     scale = 1.0 / math.sqrt(d)
-    gpu = gpu_fwd_bwd(q, k, v, do, scale, W)
+    gpu = gpu_fwd_bwd(q, k, v, do, scale, W, METHODS[method])
     rng = np.random.default_rng(5)
     for h in (0, H - 1):
         rows = sorted(set([0, 1, 127, 128, W - 1, W, W + 1, N // 2, N - 2, N - 1]
