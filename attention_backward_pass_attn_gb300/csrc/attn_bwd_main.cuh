@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(kBarAccEmpty));
       item = snake_item(k + 1, b, G, n_items);
     }
-  } else {
+  } else if (FUSED_DQ) {
     // ------------------------------------------------------------ dQ drain
     // Tensor memory -> registers -> swizzled fp32 staging tile -> TMA
     // reduce-add into the accumulator, 32 columns (16 KB) per box, two

@@ -44,6 +44,11 @@ def cuda_ready():
     assert ab.attn_last_device_error() == ab.ATTN_OK
 
 
+def assert_no_device_error(what=""):
+    st, word = ab.attn_device_error_word()
+    assert st == ab.ATTN_OK, "%s: device error status %d, word 0x%08x" % (what, st, word)
+
+
 def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
@@ -88,7 +93,7 @@ def test_workload_full_tensors(name):
     for mname, method in METHODS.items():
         gpu = gpu_fwd_bwd(q, k, v, do, w.causal, w.scale, method)
         check_full(gpu, ref, "%s dq=%s" % (name, mname))
-        assert ab.attn_last_device_error() == ab.ATTN_OK
+        assert_no_device_error("%s dq=%s" % (name, mname))
 
 
 @pytest.mark.parametrize("name", ["b1h2n128d64", "b2h16n2048d64_causal"])
@@ -122,7 +127,7 @@ def test_workload_full_size_full_tensors(name):
     for mname, method in METHODS.items():
         runs[mname] = {n: t.cpu() for n, t in
                        gpu_fwd_bwd(q, k, v, do, w.causal, w.scale, method).items()}
-        assert ab.attn_last_device_error() == ab.ATTN_OK
+        assert_no_device_error("%s dq=%s" % (name, mname))
         torch.cuda.empty_cache()
     ref = oracle.attention_forward_backward(q, k, v, do, w.causal, w.scale)
     for mname, gpu in runs.items():
