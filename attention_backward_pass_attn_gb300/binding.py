@@ -60,6 +60,7 @@ def load_library(path: str | None = None):
         sig = {
             "attn_fwd": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]),
             "attn_fwd_ex": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp]),
+            "attn_fwd_fp8": (i, [vp, vp, vp, f, f, f, vp, vp, i, i, i, i, i, f, vp]),
             "attn_bwd_workspace_size": (sz, [i, i, i, i]),
             "attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp,
@@ -168,6 +169,41 @@ def attn_fwd(q, k, v, causal: bool, scale=None, out=None, lse=None, stream=None,
                                     _doc_ptr(doc, B, N), _default_scale(d, scale),
                                     _stream(stream))
     _check("attn_fwd_ex", st)
+    return out, lse
+
+
+def _check_fp8(t: torch.Tensor, name: str, shape):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.element_size() != 1 or t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError("%s must hold e4m3 bytes (float8_e4m3fn or uint8), got %s"
+                         % (name, t.dtype))
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError("%s must be contiguous with shape %s" % (name, tuple(shape)))
+
+
+def attn_fwd_fp8(q8, k8, v8, descales, causal: bool, scale=None, out=None, lse=None,
+                 stream=None):
+    """O (bf16) and L (fp32) of exact attention over e4m3 inputs.
+
+    q8, k8, v8: e4m3 bytes [B, H, N, 128] (float8_e4m3fn or uint8 views);
+    descales: (q_descale, k_descale, v_descale), the factors that turn the
+    stored values into the values they stand for.
+    """
+    B, H, N, d = _shape4(q8, "q8")
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _check_fp8(t, n, (B, H, N, d))
+    out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None \
+        else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _check_tensor(out, "out", (B, H, N, d))
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    qd, kd, vd = (float(x) for x in descales)
+    st = load_library().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), qd, kd, vd,
+                                     out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                                     int(bool(causal)), _default_scale(d, scale),
+                                     _stream(stream))
+    _check("attn_fwd_fp8", st)
     return out, lse
 
 

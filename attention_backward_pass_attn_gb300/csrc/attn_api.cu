@@ -148,6 +148,20 @@ int make_tile_map(CUtensorMap* map, const void* ptr, const Shape& s) {
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+int make_tile_map_u8(CUtensorMap* map, const void* ptr, const Shape& s) {
+  auto encode = encode_fn();
+  if (!encode) return -1;
+  const cuuint64_t dims[3] = {cuuint64_t(s.d), cuuint64_t(s.N), cuuint64_t(s.BH)};
+  const cuuint64_t strides[2] = {cuuint64_t(s.d), cuuint64_t(s.N) * s.d};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 int make_acc_map(CUtensorMap* map, const float* acc, const Shape& s) {
   auto encode = encode_fn();
   if (!encode) return -1;
@@ -255,6 +269,30 @@ int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, 
   if (make_tile_map(&mq, Q, s) || make_tile_map(&mk, K, s) || make_tile_map(&mv, V, s))
     return ATTN_ERR_CUDA;
   return cuda_status(launch_fwd(mq, mk, mv, O, L, s, scale, err, (cudaStream_t)stream));
+}
+
+int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_descale,
+                 float k_descale, float v_descale, void* O, float* L, int B, int H, int N, int d,
+                 int causal, float scale, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!scale_ok(scale) || !scale_ok(q_descale) || !scale_ok(k_descale) || !scale_ok(v_descale))
+    return ATTN_ERR_INVALID_ARG;
+  const float score_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  if (!scale_ok(score_log2)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q8, K8, V8, O, L})) != ATTN_OK) return st;
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv;
+  if (make_tile_map_u8(&mq, Q8, s) || make_tile_map_u8(&mk, K8, s) ||
+      make_tile_map_u8(&mv, V8, s))
+    return ATTN_ERR_CUDA;
+  return cuda_status(
+      launch_fwd_fp8(mq, mk, mv, O, L, s, score_log2, v_descale, err, (cudaStream_t)stream));
 }
 
 int attn_bwd_preprocess(const void* O, const void* dO, const float* L, int B, int H, int N, int d,

@@ -92,6 +92,11 @@ Workspace carve_workspace(void* base, const Shape& s);
 // 64 x 128 x 1 box and 128-byte swizzle.  Returns 0 on success.
 int make_tile_map(CUtensorMap* map, const void* ptr, const Shape& s);
 
+// Encodes a 3-D 8-bit tensor map over a contiguous [BH][N][d] e4m3 tensor
+// (d = 128: one 128-byte row per position) with a 128 x 128 x 1 box and
+// 128-byte swizzle.  Returns 0 on success.
+int make_tile_map_u8(CUtensorMap* map, const void* ptr, const Shape& s);
+
 // Encodes a 2-D fp32 tensor map over the dQ accumulator [BH*Npad][d] with a
 // 32 x 128 box (128-byte rows) and 128-byte swizzle, for TMA reduce-add.
 int make_acc_map(CUtensorMap* map, const float* acc, const Shape& s);
@@ -103,6 +108,12 @@ cudaError_t launch_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
 // D, L log2(e) (and the document tables); zeroes the dQ accumulator only if
 // zero_acc (the fused main kernel reduces into it; the separate dQ pass does
 // not use it).
+// The e4m3 forward (head dim 128): score_log2 = scale * q_descale *
+// k_descale * log2(e); O is scaled by v_descale.
+cudaError_t launch_fwd_fp8(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, void* O, float* L, const Shape& s,
+                           float score_log2, float v_descale, int* err, cudaStream_t stream);
+
 cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
                                   const Workspace& ws, const Shape& s, bool zero_acc,
                                   cudaStream_t stream);

@@ -149,3 +149,23 @@ def make_tensor(shape, seed: int, dtype=torch.bfloat16, std: float = 1.0):
     if std != 1.0:
         t.mul_(std)
     return t.to(dtype)
+
+
+def quantize_e4m3(t: torch.Tensor):
+    """An 8-bit (OCP FP8 E4M3) copy of a tensor with one per-tensor descale
+    factor: descale = max|t| / 448 (448 is e4m3's largest finite value) as an
+    fp32 number, bytes = round-to-nearest-even(t / descale), so that
+    bytes x descale stands for t.  Returns (float8_e4m3fn tensor, descale).
+    Input preparation for the fp8 entry point: the tensors the caller hands
+    it, not attention arithmetic."""
+    x = t.to(torch.float32)
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    descale = float(torch.tensor(amax / 448.0 if amax > 0 else 1.0, dtype=torch.float32))
+    return (x / descale).to(torch.float8_e4m3fn), descale
+
+
+def make_inputs_fp8(w: Workload):
+    """The workload's seeded inputs (make_inputs, bf16) quantised to e4m3 with
+    a per-tensor descale each: ((q8, qd), (k8, kd), (v8, vd), do)."""
+    q, k, v, do = make_inputs(w)
+    return quantize_e4m3(q), quantize_e4m3(k), quantize_e4m3(v), do

@@ -321,6 +321,36 @@ def time_workload(w, steps: int, warmup: int, flush, split=False, dq_method=None
     return out
 
 
+def time_fp8_forward(w, steps: int, warmup: int, flush):
+    """attn_fwd_fp8 on the workload's inputs quantised to e4m3 (per-tensor
+    descale); per-launch CUDA-event times (ms)."""
+    import torch
+
+    from attention_backward_pass_attn_gb300 import binding as ab
+    from attention_backward_pass_attn_gb300.inputs import make_inputs_fp8
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    (q8, qd), (k8, kd), (v8, vd), _ = make_inputs_fp8(w)
+    q8, k8, v8 = q8.to(dev), k8.to(dev), v8.to(dev)
+    o = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    rec = []
+    for i in range(warmup + steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ab.attn_fwd_fp8(q8, k8, v8, (qd, kd, vd), w.causal, w.scale, out=o, lse=lse,
+                        stream=stream)
+        e1.record(stream)
+        if i >= warmup:
+            rec.append((e0, e1))
+    torch.cuda.synchronize()
+    if ab.attn_last_device_error() != ab.ATTN_OK:
+        raise RuntimeError("device error during the fp8 forward")
+    return [a.elapsed_time(b) for a, b in rec]
+
+
 def e2e_workload(w, steps: int, warmup: int):
     """The step through the public API with pinned host buffers, pipelined as a
     training loop would run it: each step copies its inputs host -> device,
@@ -530,6 +560,22 @@ def run_ours(args):
                 "faster": "reduce" if r_ms <= s_ms else "separate",
             }
         extra["dq_methods"] = cmp
+        # The e4m3 forward beside the bf16 one, against the dense fp8 peak:
+        # the measured bf16 figure times the nominal fp8/bf16 ratio (2).
+        f8 = {}
+        for name in [n for n in [w.name] + OTHER if WORKLOADS[n].d == 128]:
+            fw = WORKLOADS[name]
+            ms = statistics.median(time_fp8_forward(fw, 10, 3, flush))
+            bf = statistics.median(time_workload(fw, 10, 3, flush)["fwd"])
+            f8[name] = {"fp8_fwd_ms": round(ms, 4),
+                        "fp8_fwd_tflops": round(fw.fwd_flops() / ms / 1e9, 1),
+                        "fp8_fwd_frac_of_fp8_peak": round(fw.fwd_flops() / ms / 1e9
+                                                          / (2 * peak_tf), 4),
+                        "bf16_fwd_tflops": round(fw.fwd_flops() / bf / 1e9, 1)}
+        extra["fp8_forward"] = {"peak_tflops": 2 * peak_tf,
+                                "peak_source": "measured bf16_tflops x 2 (nominal fp8/bf16 "
+                                               "dense ratio 4.5/2.25)",
+                                "workloads": f8}
         # Mask variants: a sliding window (4096 keys) and packed documents.
         # FLOPs are those of the visible pairs: N*W - W^2/2 per head under the
         # window, the sum of n^2/2 over documents of lengths n.

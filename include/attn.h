@@ -95,6 +95,27 @@ int attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, 
                 void* stream);
 
 /*
+ * Forward with 8-bit floating-point inputs, the extension to fp8 precision
+ * that "Training Transformers and Hybrid models on AMD Instinct MI300X
+ * Accelerators" (section "Summary") names as its attention kernel's next
+ * step.  Q8, K8, V8 are OCP FP8 E4M3 bytes (torch.float8_e4m3fn), contiguous
+ * [B][H][N][d], 16-byte aligned; the values they stand for are byte value x
+ * q_descale (k_descale, v_descale), each finite and > 0.  Computes, with both
+ * contractions on the tensor core in fp8 and fp32 accumulation,
+ *
+ *   S = scale q_descale k_descale Q8 K8^T (+ mask),  L = logsumexp(S),
+ *   O = softmax(S) (v_descale V8)
+ *
+ * and writes O (bf16) and L (fp32) as attn_fwd does.  The probabilities are
+ * rounded to e4m3 (relative error up to 2^-4) for P V; the row sums and L use
+ * the unrounded fp32 values.  d must be 128 (ATTN_ERR_UNSUPPORTED otherwise);
+ * the causal mask is supported, the window and document masks are not.
+ */
+int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_descale,
+                 float k_descale, float v_descale, void* O, float* L, int B, int H, int N, int d,
+                 int causal, float scale, void* stream);
+
+/*
  * Interface utility of this library's boundary; the paper has no counterpart.
  * Bytes of device workspace attn_bwd needs for this shape (0 for an empty
  * problem).  Holds, per head, D = rowsum(dO o O) and L scaled to base 2, each

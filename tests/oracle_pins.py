@@ -532,6 +532,41 @@ def pin_doc_torch_fp64(lib):
         _close(out["dV"], tv.grad.numpy(), 1e-10, what="doc torch dV")
 
 
+# --------------------------------------------------------------------------
+# The E4M3 decoder of the fp8 path.
+# --------------------------------------------------------------------------
+def pin_e4m3_decoder(lib):
+    """The decoder against values the format's definition fixes by hand
+    (1, the largest finite 448, the smallest normal 2^-6 and subnormal 2^-9,
+    signs, NaN), against brute force over sign/exponent/mantissa, and against
+    PyTorch's own float8_e4m3fn -> float64 conversion of all 256 codes."""
+    from oracle import fp8
+
+    fixed = {0x00: 0.0, 0x38: 1.0, 0xB8: -1.0, 0x7E: 448.0, 0xFE: -448.0, 0x08: 2.0 ** -6,
+             0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x40: 2.0, 0x39: 1.125, 0x30: 0.5,
+             0x3F: 1.875, 0x77: 240.0}
+    for code, val in fixed.items():
+        assert fp8.e4m3_to_f64(code) == val, hex(code)
+    assert np.isnan(fp8.e4m3_to_f64(0x7F)) and np.isnan(fp8.e4m3_to_f64(0xFF))
+    codes = np.arange(256)
+    got = fp8.e4m3_to_f64(codes)
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            assert np.isnan(got[c])
+            continue
+        mag = (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        assert got[c] == (-mag if s else mag), hex(c)
+    try:
+        import torch
+    except ImportError:  # the cross-check needs PyTorch; the other checks stand
+        return
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    ref = ref.numpy()
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got))
+
+
 ALL_PINS = [
     pin_finite_differences,
     pin_single_key,
@@ -552,4 +587,5 @@ ALL_PINS = [
     pin_doc_single_document_is_causal,
     pin_doc_brute_force,
     pin_doc_torch_fp64,
+    pin_e4m3_decoder,
 ]

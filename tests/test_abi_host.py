@@ -153,6 +153,25 @@ def test_dq_method_and_split_steps_validation(lib):
                            None) == ab.ATTN_OK
 
 
+def test_fp8_forward_validation(lib):
+    """attn_fwd_fp8: head dim 128 only; every descale factor finite and > 0;
+    pointers checked like attn_fwd's; an empty problem launches nothing."""
+    def f8(ptr=FAKE, N=128, d=128, causal=0, qd=1.0, kd=1.0, vd=1.0, scale=0.125, q=None):
+        return lib.attn_fwd_fp8(ptr if q is None else q, ptr, ptr, qd, kd, vd, ptr, ptr, 1, 2, N,
+                                d, causal, scale, None)
+    assert f8(d=64) == ab.ATTN_ERR_UNSUPPORTED
+    assert f8(d=96) == ab.ATTN_ERR_UNSUPPORTED
+    assert f8(qd=0.0) == ab.ATTN_ERR_INVALID_ARG
+    assert f8(kd=float("inf")) == ab.ATTN_ERR_INVALID_ARG
+    assert f8(vd=float("nan")) == ab.ATTN_ERR_INVALID_ARG
+    assert f8(qd=1e30, kd=1e30) == ab.ATTN_ERR_INVALID_ARG  # combined score scale overflows
+    assert f8(scale=-1.0) == ab.ATTN_ERR_INVALID_ARG
+    assert f8(causal=5) == ab.ATTN_ERR_INVALID_ARG
+    assert f8(q=0) == ab.ATTN_ERR_INVALID_ARG
+    assert f8(q=FAKE + 4) == ab.ATTN_ERR_INVALID_ARG
+    assert f8(ptr=None, N=0) == ab.ATTN_OK
+
+
 def test_noalloc_passes_argument_errors_through(lib):
     """attn_bwd_noalloc answers every bad argument the way attn_bwd does, before
     it looks up its scratch (nothing here reaches the GPU): an unsupported head
