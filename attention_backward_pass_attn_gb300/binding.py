@@ -73,6 +73,9 @@ def load_library(path: str | None = None):
             "attn_bwd_main": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_dq_convert": (i, [vp, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_noalloc": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]),
+            "ssd_workspace_size": (sz, [i, i, i, i, i, i]),
+            "ssd_fwd": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]),
+            "ssd_bwd": (i, [vp] * 13 + [i, i, i, i, i, i, vp, sz, vp]),
             "attn_last_device_error": (i, [vp]),
             "attn_device_error_word": (i, [vp, ctypes.POINTER(ctypes.c_int)]),
             "attn_watchdog_selftest": (i, [ctypes.c_uint64, vp]),
@@ -303,3 +306,62 @@ def attn_device_error_word(stream=None):
 
 def attn_watchdog_selftest(limit_ns: int, stream=None) -> int:
     return int(load_library().attn_watchdog_selftest(int(limit_ns), _stream(stream)))
+
+
+# ------------------------------------------------------------------ Mamba-2 layer
+def _ssd_dims(x, B):
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [Bt, T, H, P] and B [Bt, T, G, N]")
+    Bt, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    return Bt, T, H, G, N, P
+
+
+def ssd_workspace(Bt, T, H, G, N, P, device) -> torch.Tensor:
+    n = max(int(load_library().ssd_workspace_size(Bt, T, H, G, N, P)), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _ssd_check_inputs(x, dt, A, B, C, D, dims):
+    Bt, T, H, G, N, P = dims
+    _check_tensor(x, "x", (Bt, T, H, P))
+    _check_tensor(B, "B", (Bt, T, G, N))
+    _check_tensor(C, "C", (Bt, T, G, N))
+    _check_tensor(dt, "dt", (Bt, T, H), torch.float32)
+    _check_tensor(A, "A", (H,), torch.float32)
+    _check_tensor(D, "D", (H,), torch.float32)
+
+
+def ssd_fwd(x, dt, A, B, C, D, y=None, workspace=None, stream=None):
+    """y [Bt, T, H, P] fp32 of the Mamba-2 state-space layer."""
+    dims = _ssd_dims(x, B)
+    _ssd_check_inputs(x, dt, A, B, C, D, dims)
+    y = torch.empty(x.shape, dtype=torch.float32, device=x.device) if y is None else y
+    _check_tensor(y, "y", x.shape, torch.float32)
+    ws = ssd_workspace(*dims, x.device) if workspace is None else workspace
+    st = load_library().ssd_fwd(x.data_ptr(), dt.data_ptr(), A.data_ptr(), B.data_ptr(),
+                                C.data_ptr(), D.data_ptr(), y.data_ptr(), *dims, ws.data_ptr(),
+                                ws.numel() * ws.element_size(), _stream(stream))
+    _check("ssd_fwd", st)
+    return y
+
+
+def ssd_bwd(x, dt, A, B, C, D, dy, workspace=None, out=None, stream=None):
+    """Gradients of <dy, y>: dict with dx, ddt, dA, dB, dC, dD (fp32)."""
+    dims = _ssd_dims(x, B)
+    _ssd_check_inputs(x, dt, A, B, C, D, dims)
+    _check_tensor(dy, "dy", x.shape)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    if out is None:
+        out = {"dx": torch.empty(x.shape, **f32), "ddt": torch.empty(dt.shape, **f32),
+               "dA": torch.empty(A.shape, **f32), "dB": torch.empty(B.shape, **f32),
+               "dC": torch.empty(C.shape, **f32), "dD": torch.empty(D.shape, **f32)}
+    ws = ssd_workspace(*dims, x.device) if workspace is None else workspace
+    st = load_library().ssd_bwd(x.data_ptr(), dt.data_ptr(), A.data_ptr(), B.data_ptr(),
+                                C.data_ptr(), D.data_ptr(), dy.data_ptr(), out["dx"].data_ptr(),
+                                out["ddt"].data_ptr(), out["dA"].data_ptr(),
+                                out["dB"].data_ptr(), out["dC"].data_ptr(),
+                                out["dD"].data_ptr(), *dims, ws.data_ptr(),
+                                ws.numel() * ws.element_size(), _stream(stream))
+    _check("ssd_bwd", st)
+    return out

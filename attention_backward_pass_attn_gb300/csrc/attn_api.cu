@@ -219,6 +219,37 @@ int auto_dq_method(const Shape& s) {
 
 }  // namespace attn
 
+namespace attn {
+namespace {
+// Validates the SSD layer's sizes; fills `empty` for a problem with no work.
+int ssd_shape(int Bt, int T, int H, int G, int N, int P, bool* empty) {
+  if (Bt < 0 || T < 0 || H < 0 || G <= 0 || N < 0 || P < 0) return ATTN_ERR_INVALID_ARG;
+  if (H % G != 0) return ATTN_ERR_INVALID_ARG;
+  if (P != 64 || (N != 64 && N != 128)) return ATTN_ERR_UNSUPPORTED;
+  const long long nc = (T + 63LL) / 64;
+  if ((long long)Bt * T * H * P > INT_MAX * 64LL || nc > INT_MAX || H > 65535 || Bt > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  *empty = (Bt == 0 || T == 0 || H == 0);
+  return ATTN_OK;
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int ssd_carve(SsdArgs* a, void* workspace, size_t bytes) {
+  const size_t need = ssd_workspace_size(a->Bt, a->T, a->H, a->G, a->N, a->P);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || bytes < need)
+    return ATTN_ERR_WORKSPACE;
+  const size_t nc = (size_t(a->T) + 63) / 64;
+  const size_t chunks = size_t(a->Bt) * a->H * nc;
+  float* base = static_cast<float*>(workspace);
+  a->ws_S = base;
+  a->ws_R = base + chunks * a->N * a->P;
+  a->ws_dec = base + 2 * chunks * a->N * a->P;
+  return ATTN_OK;
+}
+}  // namespace
+}  // namespace attn
+
 using namespace attn;
 
 extern "C" {
@@ -406,6 +437,50 @@ int attn_bwd_opts(const void* Q, const void* K, const void* V, const void* O, co
     return st;
   if (!fused) return bwd_dq_launch(Q, K, V, dO, dQ, s, scale, workspace, stream);
   return cuda_status(launch_bwd_dq_convert(dQ, ws, s, scale, (cudaStream_t)stream));
+}
+
+
+size_t ssd_workspace_size(int Bt, int T, int H, int G, int N, int P) {
+  bool empty = false;
+  if (ssd_shape(Bt, T, H, G, N, P, &empty) != ATTN_OK || empty) return 0;
+  return sizeof(float) * ssd_workspace_floats(Bt, T, H, N, P);
+}
+
+int ssd_fwd(const void* x, const float* dt, const float* A, const void* B, const void* C,
+            const float* D, float* y, int Bt, int T, int H, int G, int N, int P,
+            void* workspace, size_t workspace_bytes_, void* stream) {
+  bool empty = false;
+  int st = ssd_shape(Bt, T, H, G, N, P, &empty);
+  if (st != ATTN_OK || empty) return st;
+  if ((st = check_ptrs({x, B, C, y})) != ATTN_OK) return st;
+  if (!dt || !A || !D || !aligned4(dt) || !aligned4(A) || !aligned4(D))
+    return ATTN_ERR_INVALID_ARG;
+  SsdArgs a = {};
+  a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
+  a.Bt = Bt; a.T = T; a.H = H; a.G = G; a.N = N; a.P = P;
+  if ((st = ssd_carve(&a, workspace, workspace_bytes_)) != ATTN_OK) return st;
+  return cuda_status(launch_ssd(a, (cudaStream_t)stream));
+}
+
+int ssd_bwd(const void* x, const float* dt, const float* A, const void* B, const void* C,
+            const float* D, const void* dy, float* dx, float* ddt, float* dA, float* dB,
+            float* dC, float* dD, int Bt, int T, int H, int G, int N, int P, void* workspace,
+            size_t workspace_bytes_, void* stream) {
+  bool empty = false;
+  int st = ssd_shape(Bt, T, H, G, N, P, &empty);
+  if (st != ATTN_OK) return st;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({x, B, C, dy, dx, dB, dC})) != ATTN_OK) return st;
+  for (const void* p : {static_cast<const void*>(dt), static_cast<const void*>(A),
+                        static_cast<const void*>(D), static_cast<const void*>(ddt),
+                        static_cast<const void*>(dA), static_cast<const void*>(dD)})
+    if (!p || !aligned4(p)) return ATTN_ERR_INVALID_ARG;
+  SsdArgs a = {};
+  a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.dy = dy;
+  a.dx = dx; a.ddt = ddt; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD;
+  a.Bt = Bt; a.T = T; a.H = H; a.G = G; a.N = N; a.P = P;
+  if ((st = ssd_carve(&a, workspace, workspace_bytes_)) != ATTN_OK) return st;
+  return cuda_status(launch_ssd(a, (cudaStream_t)stream));
 }
 
 int attn_device_error_word(void* stream, int* word) {

@@ -147,4 +147,31 @@ cudaError_t launch_bwd_dq_convert(void* dQ, const Workspace& ws, const Shape& s,
 
 cudaError_t launch_watchdog_selftest(int* err, uint64_t limit_ns, cudaStream_t stream);
 
+// The Mamba-2 state-space layer (ssd.cu).  Layouts: x, dy [Bt][T][H][P] bf16;
+// dt [Bt][T][H], A, D [H] fp32; B, C [Bt][T][G][N] bf16; outputs fp32 with
+// the same layouts (dA, dD [H]).  dy == null selects the forward (y).
+struct SsdArgs {
+  const void* x;
+  const float* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* dy;
+  float* y;
+  float* dx;
+  float* ddt;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;
+  int Bt, T, H, G, N, P;
+  float* ws_S;    // [Bt][H][chunks][N][P]: chunk states, then the entering states
+  float* ws_R;    // [Bt][H][chunks][N][P]: chunk state gradients, then the leaving ones
+  float* ws_dec;  // [Bt][H][chunks]: each chunk's total decay
+};
+cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t stream);
+// Floats of workspace the layer needs (both scans' states plus the decays).
+size_t ssd_workspace_floats(int Bt, int T, int H, int N, int P);
+
 }  // namespace attn

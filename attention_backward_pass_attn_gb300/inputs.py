@@ -169,3 +169,59 @@ def make_inputs_fp8(w: Workload):
     a per-tensor descale each: ((q8, qd), (k8, kd), (v8, vd), do)."""
     q, k, v, do = make_inputs(w)
     return quantize_e4m3(q), quantize_e4m3(k), quantize_e4m3(v), do
+
+
+# --------------------------------------------------------------------------
+# The Mamba-2 state-space layer (the hybrid model's second hot kernel).
+# --------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class SsdWorkload:
+    """Shapes of one Mamba-2 layer: Bt sequences of T steps, H heads of P
+    channels, G groups of B/C with a state of N per channel."""
+    name: str
+    Bt: int
+    T: int
+    H: int
+    G: int
+    N: int
+    P: int
+    seed: int
+
+    @property
+    def tokens(self) -> int:
+        return self.Bt * self.T
+
+    def recurrence_flops(self) -> float:
+        """FLOPs of the backward written as the recurrence and its adjoint:
+        per (b, t, h) the state update and the suffix update (2 NP each),
+        dx, dB, dC (2 NP each), ddt and dA (5 NP), the recomputed forward
+        state (2 NP): 17 N P."""
+        return 17.0 * self.Bt * self.T * self.H * self.N * self.P
+
+
+SSD_WORKLOADS = {
+    # d_model 2048 with expansion 2 (4096 channels = 64 heads of 64), state
+    # 128, one group: at the three sequence lengths the pages measure.
+    "ssd_b2t2048h64n128": SsdWorkload("ssd_b2t2048h64n128", 2, 2048, 64, 1, 128, 64, seed=21),
+    "ssd_b2t4096h64n128": SsdWorkload("ssd_b2t4096h64n128", 2, 4096, 64, 1, 128, 64, seed=22),
+    "ssd_b1t8192h64n128": SsdWorkload("ssd_b1t8192h64n128", 1, 8192, 64, 1, 128, 64, seed=23),
+}
+
+
+def make_ssd_inputs(w: SsdWorkload):
+    """(x, dt, A, B, C, D, dy) as CPU tensors: x, B, C, dy standard normal,
+    rounded once to bf16; dt log-uniform in [1e-3, 1e-1] and A uniform in
+    [-16, -1] (Mamba-2's initialisation ranges), D uniform in [0.5, 1.5], all
+    fp32."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed))
+    x = torch.randn((w.Bt, w.T, w.H, w.P), generator=g, dtype=torch.float32)
+    B = torch.randn((w.Bt, w.T, w.G, w.N), generator=g, dtype=torch.float32)
+    C = torch.randn((w.Bt, w.T, w.G, w.N), generator=g, dtype=torch.float32)
+    dy = torch.randn((w.Bt, w.T, w.H, w.P), generator=g, dtype=torch.float32)
+    u = torch.rand((w.Bt, w.T, w.H), generator=g, dtype=torch.float32)
+    dt = torch.exp(math.log(1e-3) + u * (math.log(1e-1) - math.log(1e-3)))
+    A = -(1.0 + 15.0 * torch.rand((w.H,), generator=g, dtype=torch.float32))
+    D = 0.5 + torch.rand((w.H,), generator=g, dtype=torch.float32)
+    bf = torch.bfloat16
+    return x.to(bf), dt, A, B.to(bf), C.to(bf), D, dy.to(bf)

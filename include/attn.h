@@ -253,6 +253,43 @@ int attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                      int causal, float scale, void* stream);
 
 /*
+ * The Mamba-2 state-space layer, the hybrid model's second hot kernel beside
+ * attention ("Training Transformers and Hybrid models on AMD Instinct MI300X
+ * Accelerators", section "Mamba-2": its backward by a prefix scan, a reverse
+ * scan, and block reductions finished with atomic adds).  Per batch element b
+ * and head h, with B and C from group g = h / (H / G) and a state h_t of
+ * N x P values:
+ *
+ *   h_t = exp(dt_t A_h) h_{t-1} + dt_t B_t x_t^T,  h_{-1} = 0
+ *   y_t = h_t^T C_t + D_h x_t
+ *
+ * Layouts (contiguous): x, dy [Bt][T][H][P] bf16; dt [Bt][T][H] fp32 (the
+ * step sizes, already positive); A, D [H] fp32; B, C [Bt][T][G][N] bf16.
+ * Outputs fp32: y, dx [Bt][T][H][P]; ddt [Bt][T][H]; dA, dD [H];
+ * dB, dC [Bt][T][G][N].  P must be 64 and N 64 or 128 (else
+ * ATTN_ERR_UNSUPPORTED); H a multiple of G; bf16 and fp32 arrays 16- and
+ * 4-byte aligned.  All pointers are device pointers; the workspace
+ * (ssd_workspace_size bytes, 256-byte aligned) is the caller's.  Sums over
+ * heads (dB, dC of a group) and over time (dA, dD) use fp32 atomic adds, so
+ * their last bits vary between runs.
+ */
+size_t ssd_workspace_size(int Bt, int T, int H, int G, int N, int P);
+
+/* Forward: y of the layer above. */
+int ssd_fwd(const void* x, const float* dt, const float* A, const void* B, const void* C,
+            const float* D, float* y, int Bt, int T, int H, int G, int N, int P,
+            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward for the loss <dy, y>: dx, ddt, dA, dB, dC, dD (overwritten, not
+ * accumulated into).  Recomputes the states from the inputs; y is not needed.
+ */
+int ssd_bwd(const void* x, const float* dt, const float* A, const void* B, const void* C,
+            const float* D, const void* dy, float* dx, float* ddt, float* dA, float* dB,
+            float* dC, float* dD, int Bt, int T, int H, int G, int N, int P, void* workspace,
+            size_t workspace_bytes, void* stream);
+
+/*
  * Interface utility of this library's boundary (failure detection); the paper
  * has no counterpart.
  * Synchronise `stream`, then read and clear the current device's error word.

@@ -32,10 +32,10 @@
  *
  * How.  Pass 1 runs the recurrence forward and keeps every h_t of the head
  * (T x N x P doubles); pass 2 runs the suffix recurrence backward and forms
- * the gradients from it.  Threads (OpenMP) take (batch, group) pairs, each
- * handling the heads of its group in order, so every output element is
- * written by one thread; dA and dD are summed per (batch, head) and then
- * over batches in a fixed order.  Results do not depend on the thread count.
+ * the gradients from it.  Threads (OpenMP) take (batch, head) pairs; every
+ * per-head quantity is written by one thread, and the sums over heads (dB,
+ * dC of a group) and over batches (dA, dD) are taken afterwards in a fixed
+ * order, so results do not depend on the thread count.
  *
  * Layout (contiguous, row-major doubles):
  *   x, y, dy, dx    [Bt][T][H][P]
@@ -138,18 +138,26 @@ int oracle_ssd_fwd_bwd(const double *x, const double *dt, const double *A, const
     return SSD_ERR_ARG;
   set_threads(nthreads);
   const long hpg = H / G;
-  /* per (b, h) partial sums of dA and dD, added over b in order afterwards */
+  /* per (b, h) partials: dA, dD, and dB, dC [Bt][H][T][N], summed over the
+   * heads of each group (and dA, dD over batches) in a fixed order below */
   double *pA = (double *)calloc((size_t)(Bt * H), sizeof(double));
   double *pD = (double *)calloc((size_t)(Bt * H), sizeof(double));
-  if (!pA || !pD) {
+  double *pB = (double *)calloc((size_t)(Bt * H * T * N > 0 ? Bt * H * T * N : 1),
+                                sizeof(double));
+  double *pC = (double *)calloc((size_t)(Bt * H * T * N > 0 ? Bt * H * T * N : 1),
+                                sizeof(double));
+  if (!pA || !pD || !pB || !pC) {
     free(pA);
     free(pD);
+    free(pB);
+    free(pC);
     return SSD_ERR_NOMEM;
   }
   int failed = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
   for (long b = 0; b < Bt; ++b)
-    for (long g = 0; g < G; ++g) {
+    for (long h = 0; h < H; ++h) {
+      const long g = h / hpg;
       double *hs = (double *)malloc(sizeof(double) * (size_t)(T * N * P > 0 ? T * N * P : 1));
       double *gs = (double *)malloc(sizeof(double) * (size_t)(N * P > 0 ? N * P : 1));
       if (!hs || !gs) {
@@ -159,65 +167,71 @@ int oracle_ssd_fwd_bwd(const double *x, const double *dt, const double *A, const
         failed = 1;
         continue;
       }
-      /* dB, dC of this (b, g) start at zero and collect every head of g */
-      for (long t = 0; t < T; ++t)
+      const double Ah = A[h], Dh = D[h];
+      scan_forward(x, dt, Ah, Bm, Cm, Dh, b, h, g, T, H, G, N, P, hs, y);
+      memset(gs, 0, sizeof(double) * (size_t)(N * P)); /* g_T = 0 */
+      double sumA = 0.0, sumD = 0.0;
+      double a_next = 0.0; /* a_{t+1}; unused at t = T - 1 (g_T = 0) */
+      for (long t = T - 1; t >= 0; --t) {
+        const double d = dt[(b * T + t) * H + h];
+        const double a = exp(d * Ah);
+        const double *xt = x + ((b * T + t) * H + h) * P;
+        const double *dyt = dy + ((b * T + t) * H + h) * P;
+        const double *Bt_ = Bm + ((b * T + t) * G + g) * N;
+        const double *Ct = Cm + ((b * T + t) * G + g) * N;
+        const double *ht = hs + t * N * P;
+        const double *hp = t > 0 ? hs + (t - 1) * N * P : NULL;
+        /* g_t = C_t dy_t^T + a_{t+1} g_{t+1} */
+        for (long n = 0; n < N; ++n)
+          for (long p = 0; p < P; ++p) gs[n * P + p] = Ct[n] * dyt[p] + a_next * gs[n * P + p];
+        double *dxt = dx + ((b * T + t) * H + h) * P;
+        for (long p = 0; p < P; ++p) {
+          double acc = 0.0;
+          for (long n = 0; n < N; ++n) acc += gs[n * P + p] * Bt_[n];
+          dxt[p] = d * acc + Dh * dyt[p];
+        }
+        double *dBt = pB + ((b * H + h) * T + t) * N;
+        double *dCt = pC + ((b * H + h) * T + t) * N;
         for (long n = 0; n < N; ++n) {
-          dB[((b * T + t) * G + g) * N + n] = 0.0;
-          dC[((b * T + t) * G + g) * N + n] = 0.0;
-        }
-      for (long h = g * hpg; h < (g + 1) * hpg; ++h) {
-        const double Ah = A[h], Dh = D[h];
-        scan_forward(x, dt, Ah, Bm, Cm, Dh, b, h, g, T, H, G, N, P, hs, y);
-        memset(gs, 0, sizeof(double) * (size_t)(N * P));  /* g_T = 0 */
-        double sumA = 0.0, sumD = 0.0;
-        double a_next = 0.0;  /* a_{t+1}; unused at t = T - 1 (g_T = 0) */
-        for (long t = T - 1; t >= 0; --t) {
-          const double d = dt[(b * T + t) * H + h];
-          const double a = exp(d * Ah);
-          const double *xt = x + ((b * T + t) * H + h) * P;
-          const double *dyt = dy + ((b * T + t) * H + h) * P;
-          const double *Bt = Bm + ((b * T + t) * G + g) * N;
-          const double *Ct = Cm + ((b * T + t) * G + g) * N;
-          const double *ht = hs + t * N * P;
-          const double *hp = t > 0 ? hs + (t - 1) * N * P : NULL;
-          /* g_t = C_t dy_t^T + a_{t+1} g_{t+1} */
-          for (long n = 0; n < N; ++n)
-            for (long p = 0; p < P; ++p) gs[n * P + p] = Ct[n] * dyt[p] + a_next * gs[n * P + p];
-          double *dxt = dx + ((b * T + t) * H + h) * P;
+          double accb = 0.0, accc = 0.0;
           for (long p = 0; p < P; ++p) {
-            double acc = 0.0;
-            for (long n = 0; n < N; ++n) acc += gs[n * P + p] * Bt[n];
-            dxt[p] = d * acc + Dh * dyt[p];
+            accb += gs[n * P + p] * xt[p];
+            accc += ht[n * P + p] * dyt[p];
           }
-          double *dBt = dB + ((b * T + t) * G + g) * N;
-          double *dCt = dC + ((b * T + t) * G + g) * N;
-          for (long n = 0; n < N; ++n) {
-            double accb = 0.0, accc = 0.0;
-            for (long p = 0; p < P; ++p) {
-              accb += gs[n * P + p] * xt[p];
-              accc += ht[n * P + p] * dyt[p];
-            }
-            dBt[n] += d * accb;
-            dCt[n] += accc;
-          }
-          double dd = 0.0, da = 0.0;
-          for (long n = 0; n < N; ++n)
-            for (long p = 0; p < P; ++p) {
-              const double prev = hp ? hp[n * P + p] : 0.0;
-              dd += gs[n * P + p] * (Ah * a * prev + Bt[n] * xt[p]);
-              da += gs[n * P + p] * d * a * prev;
-            }
-          ddt[(b * T + t) * H + h] = dd;
-          sumA += da;
-          for (long p = 0; p < P; ++p) sumD += dyt[p] * xt[p];
-          a_next = a;
+          dBt[n] = d * accb;
+          dCt[n] = accc;
         }
-        pA[b * H + h] = sumA;
-        pD[b * H + h] = sumD;
+        double dd = 0.0, da = 0.0;
+        for (long n = 0; n < N; ++n)
+          for (long p = 0; p < P; ++p) {
+            const double prev = hp ? hp[n * P + p] : 0.0;
+            dd += gs[n * P + p] * (Ah * a * prev + Bt_[n] * xt[p]);
+            da += gs[n * P + p] * d * a * prev;
+          }
+        ddt[(b * T + t) * H + h] = dd;
+        sumA += da;
+        for (long p = 0; p < P; ++p) sumD += dyt[p] * xt[p];
+        a_next = a;
       }
+      pA[b * H + h] = sumA;
+      pD[b * H + h] = sumD;
       free(hs);
       free(gs);
     }
+  /* dB, dC: the sum over the heads of each group, in head order */
+#pragma omp parallel for collapse(2) schedule(static)
+  for (long b = 0; b < Bt; ++b)
+    for (long t = 0; t < T; ++t)
+      for (long g = 0; g < G; ++g)
+        for (long n = 0; n < N; ++n) {
+          double sb = 0.0, sc = 0.0;
+          for (long h = g * hpg; h < (g + 1) * hpg; ++h) {
+            sb += pB[((b * H + h) * T + t) * N + n];
+            sc += pC[((b * H + h) * T + t) * N + n];
+          }
+          dB[((b * T + t) * G + g) * N + n] = sb;
+          dC[((b * T + t) * G + g) * N + n] = sc;
+        }
   for (long h = 0; h < H; ++h)
     for (long b = 0; b < Bt; ++b) {
       dA[h] += pA[b * H + h];
@@ -225,6 +239,8 @@ int oracle_ssd_fwd_bwd(const double *x, const double *dt, const double *A, const
     }
   free(pA);
   free(pD);
+  free(pB);
+  free(pC);
   return failed ? SSD_ERR_NOMEM : SSD_OK;
 }
 

@@ -172,6 +172,32 @@ def test_fp8_forward_validation(lib):
     assert f8(ptr=None, N=0) == ab.ATTN_OK
 
 
+def test_ssd_validation(lib):
+    """The Mamba-2 layer: P = 64 and N in {64, 128} only, heads a multiple of
+    groups, pointers and workspace checked before any launch."""
+    ws_need = lib.ssd_workspace_size(1, 128, 2, 1, 128, 64)
+    assert ws_need > 0 and ws_need % 4 == 0
+    assert lib.ssd_workspace_size(1, 128, 2, 1, 128, 32) == 0
+    assert lib.ssd_workspace_size(1, 0, 2, 1, 128, 64) == 0
+
+    def bwd_(Bt=1, T=128, H=2, G=1, N=128, P=64, ptr=FAKE, ws=FAKE, wsb=None, dt=FAKE):
+        wsb = ws_need if wsb is None else wsb
+        return lib.ssd_bwd(ptr, dt, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr,
+                           Bt, T, H, G, N, P, ws, wsb, None)
+    assert bwd_(P=32) == ab.ATTN_ERR_UNSUPPORTED
+    assert bwd_(N=96) == ab.ATTN_ERR_UNSUPPORTED
+    assert bwd_(H=3, G=2) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd_(G=0) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd_(T=-1) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd_(ptr=None) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd_(dt=FAKE + 2) == ab.ATTN_ERR_INVALID_ARG
+    assert bwd_(ws=None) == ab.ATTN_ERR_WORKSPACE
+    assert bwd_(wsb=ws_need - 4) == ab.ATTN_ERR_WORKSPACE
+    assert bwd_(ptr=None, T=0, ws=None, wsb=0, dt=None) == ab.ATTN_OK
+    assert lib.ssd_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 1, 128, 64, FAKE,
+                       ws_need, None) == ab.ATTN_ERR_INVALID_ARG
+
+
 def test_noalloc_passes_argument_errors_through(lib):
     """attn_bwd_noalloc answers every bad argument the way attn_bwd does, before
     it looks up its scratch (nothing here reaches the GPU): an unsupported head

@@ -46,16 +46,17 @@ MUTANTS = {
     "carry_without_decay": ("+ a_next * gs[n * P + p];", "+ gs[n * P + p];"),
     "dx_missing_dt": ("dxt[p] = d * acc + Dh * dyt[p];", "dxt[p] = acc + Dh * dyt[p];"),
     "dx_missing_skip": ("dxt[p] = d * acc + Dh * dyt[p];", "dxt[p] = d * acc;"),
-    "db_missing_dt": ("dBt[n] += d * accb;", "dBt[n] += accb;"),
+    "db_missing_dt": ("dBt[n] = d * accb;", "dBt[n] = accb;"),
     "dc_uses_previous_state": ("accc += ht[n * P + p] * dyt[p];",
                                "accc += (hp ? hp[n * P + p] : 0.0) * dyt[p];"),
-    "ddt_drops_decay_term": ("dd += gs[n * P + p] * (Ah * a * prev + Bt[n] * xt[p]);",
-                             "dd += gs[n * P + p] * (Bt[n] * xt[p]);"),
+    "ddt_drops_decay_term": ("dd += gs[n * P + p] * (Ah * a * prev + Bt_[n] * xt[p]);",
+                             "dd += gs[n * P + p] * (Bt_[n] * xt[p]);"),
     "da_sign_flip": ("sumA += da;", "sumA -= da;"),
     "forward_decay_off_by_one": ("const double a = exp(d * A);", "const double a = exp(A);"),
     "group_index_wrong": ("scan_forward(x, dt, A[h], Bm, Cm, D[h], b, h, h / hpg,",
                           "scan_forward(x, dt, A[h], Bm, Cm, D[h], b, h, 0,"),
-    "groups_not_summed": ("dCt[n] += accc;", "dCt[n] = accc;"),
+    "groups_not_summed": ("for (long h = g * hpg; h < (g + 1) * hpg; ++h) {\n            sb",
+                          "for (long h = g * hpg; h < g * hpg + 1; ++h) {\n            sb"),
 }
 
 
