@@ -351,6 +351,52 @@ def time_fp8_forward(w, steps: int, warmup: int, flush):
     return [a.elapsed_time(b) for a, b in rec]
 
 
+def time_ssd(w, steps: int, warmup: int, flush):
+    """ssd_fwd and ssd_bwd of one Mamba-2 layer shape: per-call CUDA-event
+    times (ms) of each, L2 flushed before every call."""
+    import torch
+
+    from attention_backward_pass_attn_gb300 import binding as ab
+    from attention_backward_pass_attn_gb300.inputs import make_ssd_inputs
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x, dt, A, B, C, D, dy = (t.to(dev) for t in make_ssd_inputs(w))
+    ws = ab.ssd_workspace(w.Bt, w.T, w.H, w.G, w.N, w.P, dev)
+    y = torch.empty(x.shape, dtype=torch.float32, device=dev)
+    out = None
+    stream = torch.cuda.current_stream()
+    fwd, bwd = [], []
+    for i in range(warmup + steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush()
+        ev[0].record(stream)
+        ab.ssd_fwd(x, dt, A, B, C, D, y=y, workspace=ws, stream=stream)
+        ev[1].record(stream)
+        flush()
+        ev[2].record(stream)
+        out = ab.ssd_bwd(x, dt, A, B, C, D, dy, workspace=ws, out=out, stream=stream)
+        ev[3].record(stream)
+        if i >= warmup:
+            fwd.append(ev)
+    torch.cuda.synchronize()
+    if ab.attn_last_device_error() != ab.ATTN_OK:
+        raise RuntimeError("device error during the state-space layer")
+    return ([e[0].elapsed_time(e[1]) for e in fwd], [e[2].elapsed_time(e[3]) for e in fwd])
+
+
+def ssd_chunked_flops(w, chunk: int = 64):
+    """FLOPs the chunked backward executes (the kernels' own algorithm):
+    per chunk of L steps, the chunk states S and R (4 L N P), the scans over
+    chunks (4 N P), and the chunk gradients: C B^T and dy x^T (2 L^2 (N+P)),
+    the triangular products for dx, dB, dC (L^2 P + 2 L^2 N) and their state
+    terms (6 L N P), <dH, H> (2 N P)."""
+    L, N, P = chunk, w.N, w.P
+    nc = (w.T + L - 1) // L
+    per = 4 * L * N * P + 4 * N * P + 2 * L * L * (N + P) + L * L * P + 2 * L * L * N \
+        + 6 * L * N * P + 2 * N * P
+    return float(per) * w.Bt * w.H * nc
+
+
 def e2e_workload(w, steps: int, warmup: int):
     """The step through the public API with pinned host buffers, pipelined as a
     training loop would run it: each step copies its inputs host -> device,
@@ -576,6 +622,24 @@ def run_ours(args):
                                 "peak_source": "measured bf16_tflops x 2 (nominal fp8/bf16 "
                                                "dense ratio 4.5/2.25)",
                                 "workloads": f8}
+        # The Mamba-2 layer of the hybrid model: fp32 arithmetic on the CUDA
+        # cores, so its peak is the fp32 FMA rate: 152 SMs x 128 lanes x 2
+        # FLOP x the SM clock (2070 MHz maximum).
+        from attention_backward_pass_attn_gb300.inputs import SSD_WORKLOADS
+        alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        ssd_res = {}
+        for name, sw in SSD_WORKLOADS.items():
+            f_ms, b_ms = time_ssd(sw, 10, 3, flush)
+            fm, bm = statistics.median(f_ms), statistics.median(b_ms)
+            ssd_res[name] = {
+                "fwd_ms": round(fm, 4), "bwd_ms": round(bm, 4),
+                "bwd_tokens_per_s": round(sw.tokens / (bm * 1e-3), 1),
+                "bwd_recurrence_tflops": round(sw.recurrence_flops() / bm / 1e9, 2),
+                "bwd_chunked_tflops": round(ssd_chunked_flops(sw) / bm / 1e9, 2),
+                "bwd_alu_frac": round(ssd_chunked_flops(sw) / bm / 1e9 / alu_peak, 4)}
+        extra["ssd"] = {"alu_peak_tflops": round(alu_peak, 1),
+                        "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                        "workloads": ssd_res}
         # Mask variants: a sliding window (4096 keys) and packed documents.
         # FLOPs are those of the visible pairs: N*W - W^2/2 per head under the
         # window, the sum of n^2/2 over documents of lengths n.
