@@ -61,7 +61,8 @@ struct SLayout {
   static constexpr int oM1 = odH + N * HS;
   static constexpr int oM2 = oM1 + Lc * MS;
   static constexpr int oVec = oM2 + Lc * MS;  // kVecs vectors of Lc
-  static constexpr int oRed = oVec + kVecs * Lc;
+  static constexpr int oColPart = oVec + kVecs * Lc;  // [16][Lc] partial column sums
+  static constexpr int oRed = oColPart + 16 * Lc;
   static constexpr int kFloats = oRed + 8;
   static constexpr int kBytes = kFloats * 4;
 };
@@ -339,10 +340,20 @@ __global__ void __launch_bounds__(kThreads)
       const float s = sum16(row[a]);
       if (tx == 0) vec[vROW * Lc + i0 + a] = s;  // one writer per row
     }
+    // column sums over the 16 row blocks, added in a fixed order below so
+    // that ddt is bitwise repeatable
+    float* colpart = sm + Ly::oColPart;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) atomicAdd(&vec[vCOL * Lc + j0 + q], col[q]);
+    for (int q = 0; q < 4; ++q) colpart[ty * Lc + j0 + q] = col[q];
   }
   __syncthreads();
+  if (threadIdx.x < Lc) {
+    const float* colpart = sm + Ly::oColPart;
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) s += colpart[r * Lc + threadIdx.x];
+    vec[vCOL * Lc + threadIdx.x] = s;
+  }
 
   // ---- B: dx_j = dt_j (sum_i M1[i][j] dy_i + e_out[j] dH^T B_j) + D dy_j
   {

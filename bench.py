@@ -99,17 +99,31 @@ def _strip_comments(src: str) -> str:
     return "\n".join(ln for ln in lines if ln.strip())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources, comments excluded: a stored ncu traffic
-    figure is only used if the kernels' code has not changed since it was
-    captured."""
+# The CUDA sources each profiled kernel is built from (its own code, the
+# PTX wrappers and mask helpers it includes, and its launcher).
+KERNEL_SOURCES = {
+    "attn_bwd_main_kernel": ["attn_bwd_main.cuh", "attn_bwd.cu", "ptx.cuh", "mask.cuh"],
+    "attn_bwd_preprocess_kernel": ["attn_bwd.cu", "attn_bwd_main.cuh", "ptx.cuh", "mask.cuh"],
+    "attn_bwd_dq_convert_kernel": ["attn_bwd.cu", "attn_bwd_main.cuh", "ptx.cuh", "mask.cuh"],
+    "attn_fwd_kernel": ["attn_fwd.cu", "ptx.cuh", "mask.cuh"],
+    "attn_fwd_fp8_kernel": ["attn_fwd_fp8.cu", "ptx.cuh"],
+    "ssd_chunk_bwd_kernel": ["ssd.cu", "ptx.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the CUDA sources a kernel is built from (all of them when no
+    kernel is named), comments excluded: a stored ncu traffic figure is only
+    used if that code has not changed since it was captured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_backward_pass_attn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), encoding="utf-8") as f:
-                code = _strip_comments(f.read())
-            h.update(name.encode() + b"\0" + code.encode())
+    names = KERNEL_SOURCES.get(kernel) if kernel else None
+    if names is None:
+        names = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h"))]
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            code = _strip_comments(f.read())
+        h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
@@ -124,7 +138,7 @@ def stored_ncu(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     ent = table.get("%s@%s" % (kernel, workload))
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent
 
@@ -727,6 +741,39 @@ def run_ours(args):
     return line
 
 
+def run_leg(args):
+    """One leg alone (the e4m3 forward, the backward with the separate dQ
+    pass, or the Mamba-2 layer) on --workload, W + K calls, for profiler
+    captures of those kernels; prints their median CUDA-event times."""
+    import torch
+
+    torch.cuda.set_device(0)
+    from attention_backward_pass_attn_gb300 import binding as ab
+    from attention_backward_pass_attn_gb300.inputs import SSD_WORKLOADS
+
+    ab.load_library()
+    dev = torch.device("cuda", 0)
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    steps, warm = max(args.steps, 1), max(args.warmup, 3)
+    if args.leg == "ssd":
+        w = SSD_WORKLOADS[args.workload]
+        f_ms, b_ms = time_ssd(w, steps, warm, flush)
+        return {"leg": "ssd", "workload": w.name, "fwd_ms": statistics.median(f_ms),
+                "bwd_ms": statistics.median(b_ms)}
+    w = workload_of(args)
+    if args.leg == "fp8_forward":
+        ms = statistics.median(time_fp8_forward(w, steps, warm, flush))
+        return {"leg": "fp8_forward", "workload": w.name, "ms": ms,
+                "tflops": w.fwd_flops() / ms / 1e9}
+    r = time_workload(w, steps, warm, flush, split=True, dq_method=ab.ATTN_DQ_SEPARATE)
+    return {"leg": "dq_separate", "workload": w.name,
+            "main_dkdv_ms": statistics.median(r["main"]), "dq_ms": statistics.median(r["conv"])}
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm.  Each step evaluates a bounded
@@ -804,10 +851,17 @@ def main(argv=None):
                         "case of the same kernels, for profiler captures); 0 = as named")
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--leg", default="attention",
+                   choices=["attention", "fp8_forward", "dq_separate", "ssd"],
+                   help="run one other leg alone on --workload (for profiler captures); "
+                        "prints its timing, not the benchmark line")
     args = p.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         p.error("--warmup must be >= 3")
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.leg != "attention":
+        line = run_leg(args)
+    else:
+        line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
     try:

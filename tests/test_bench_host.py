@@ -75,13 +75,31 @@ def test_stored_traffic_requires_current_sources(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "current")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel=None: "current")
     (prof / "ncu_traffic.json").write_text(json.dumps({
         "k@w": {"source_hash": "stale", "dram_bytes_per_launch": 123},
         "k2@w": {"source_hash": "current", "dram_bytes_per_launch": 456}}))
     assert bench.stored_traffic("k", "w") is None
     assert bench.stored_traffic("k2", "w") == 456
     assert bench.stored_traffic("missing", "w") is None
+
+
+def test_kernel_hash_covers_its_sources(tmp_path, monkeypatch):
+    """A kernel's hash changes with its own sources and ignores comments and
+    the files it is not built from."""
+    csrc = tmp_path / "attention_backward_pass_attn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", {"k": ["a.cu", "p.cuh"]})
+    (csrc / "a.cu").write_text("int a = 1;  // note\n")
+    (csrc / "p.cuh").write_text("#pragma once\n")
+    (csrc / "other.cu").write_text("int b = 2;\n")
+    h0 = bench.kernel_source_hash("k")
+    (csrc / "a.cu").write_text("int a = 1;  // another note\n")
+    (csrc / "other.cu").write_text("int b = 3;\n")
+    assert bench.kernel_source_hash("k") == h0
+    (csrc / "a.cu").write_text("int a = 2;\n")
+    assert bench.kernel_source_hash("k") != h0
 
 
 def test_reference_arm_runs_on_cpu():
