@@ -239,12 +239,19 @@ int ssd_carve(SsdArgs* a, void* workspace, size_t bytes) {
   const size_t need = ssd_workspace_size(a->Bt, a->T, a->H, a->G, a->N, a->P);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || bytes < need)
     return ATTN_ERR_WORKSPACE;
+  auto r64 = [](size_t v) { return (v + 63) / 64 * 64; };
   const size_t nc = (size_t(a->T) + 63) / 64;
   const size_t chunks = size_t(a->Bt) * a->H * nc;
-  float* base = static_cast<float*>(workspace);
-  a->ws_S = base;
-  a->ws_R = base + chunks * a->N * a->P;
-  a->ws_dec = base + 2 * chunks * a->N * a->P;
+  const size_t states = r64(chunks * a->N * a->P);
+  const size_t heads = r64(size_t(a->Bt) * a->T * a->H * a->N);
+  float* p = static_cast<float*>(workspace);
+  a->ws_S = p;
+  a->ws_R = p += states;
+  a->ws_dBh = p += states;
+  a->ws_dCh = p += heads;
+  a->ws_dec = p += heads;
+  a->ws_dA = p += r64(chunks);
+  a->ws_dD = p += r64(chunks);
   return ATTN_OK;
 }
 }  // namespace

@@ -166,9 +166,13 @@ struct SsdArgs {
   float* dC;
   float* dD;
   int Bt, T, H, G, N, P;
-  float* ws_S;    // [Bt][H][chunks][N][P]: chunk states, then the entering states
-  float* ws_R;    // [Bt][H][chunks][N][P]: chunk state gradients, then the leaving ones
+  float* ws_S;    // [Bt][H][chunks][P][N]: chunk states, then the entering states
+  float* ws_R;    // [Bt][H][chunks][P][N]: chunk state gradients, then the leaving ones
+  float* ws_dBh;  // [Bt][T][H][N]: each head's dB, summed over a group's heads after
+  float* ws_dCh;  // [Bt][T][H][N]: each head's dC
   float* ws_dec;  // [Bt][H][chunks]: each chunk's total decay
+  float* ws_dA;   // [Bt][H][chunks]: each chunk's share of dA
+  float* ws_dD;   // [Bt][H][chunks]: each chunk's share of dD
 };
 cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t stream);
 // Floats of workspace the layer needs (both scans' states plus the decays).

@@ -270,8 +270,8 @@ int attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
  * ATTN_ERR_UNSUPPORTED); H a multiple of G; bf16 and fp32 arrays 16- and
  * 4-byte aligned.  All pointers are device pointers; the workspace
  * (ssd_workspace_size bytes, 256-byte aligned) is the caller's.  Sums over
- * heads (dB, dC of a group) and over time (dA, dD) use fp32 atomic adds, so
- * their last bits vary between runs.
+ * heads (dB, dC of a group) and over time (dA, dD) run in a fixed order, so
+ * every output is bitwise repeatable.
  */
 size_t ssd_workspace_size(int Bt, int T, int H, int G, int N, int P);
 

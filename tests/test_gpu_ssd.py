@@ -90,10 +90,10 @@ def test_ssd_workloads_full_tensors(name):
 
 
 def test_ssd_repeatable_and_no_stale_state():
-    """dx and ddt (one writer per element) are bitwise repeatable and the
-    atomic sums repeat within rounding, with the same workspace and output
-    buffers reused after a call on different inputs (the gradients are
-    overwritten, not accumulated into)."""
+    """Every output is bitwise repeatable (each element has one writer, and
+    the sums over heads, batches and chunks run in a fixed order), with the
+    same workspace and output buffers reused after a call on different
+    inputs (the gradients are overwritten, not accumulated into)."""
     dev = torch.device("cuda", 0)
     ws = ab.ssd_workspace(2, 300, 4, 2, 128, 64, dev)
     out = None
@@ -105,8 +105,6 @@ def test_ssd_repeatable_and_no_stale_state():
         torch.cuda.synchronize()
         res.append({k: v.cpu().numpy().astype(np.float64) for k, v in out.items()})
     a, b = res[0], res[2]
-    for k in ("dx", "ddt"):
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD"):
         assert np.array_equal(a[k], b[k]), k
-    for k in ("dA", "dB", "dC", "dD"):
-        assert rel(a[k], b[k]) <= 1e-5, k
     assert ab.attn_last_device_error() == ab.ATTN_OK
