@@ -282,9 +282,9 @@ __global__ void __launch_bounds__(kThreads)
   grid_dep_launch();
   if (e >= NP) return;
   const size_t base = (size_t(b) * d.H + h) * d.nc;
-  // Eight chunks' values are loaded before any is used: the loads do not
+  // Sixteen chunks' values are loaded before any is used: the loads do not
   // depend on the carry, only the multiply-adds do.
-  constexpr int U = 8;
+  constexpr int U = 16;
   float carry = 0.f;
   for (int c0 = 0; c0 < d.nc; c0 += U) {
     float v[U], a[U];
