@@ -80,6 +80,10 @@ def load(path: str | None = None):
                                               ctypes.c_double, L, lp, L, lp, dp, dp, dp,
                                               dp, dp, ctypes.c_int]
         lib.oracle_attn_head_rows.restype = ctypes.c_int
+        lib.oracle_attn_bwd_budget.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, ctypes.c_int,
+                                               ctypes.c_double, dp, dp, dp, dp, dp,
+                                               ctypes.c_int]
+        lib.oracle_attn_bwd_budget.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         if path is None:
@@ -192,4 +196,27 @@ def attention_head_rows(q, k, v, do, causal: bool, scale: float, q_rows, k_rows,
         _ptr(out["L"]), _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), int(threads))
     if st != 0:
         raise RuntimeError("oracle_attn_head_rows failed with status %d" % st)
+    return out
+
+
+def backward_rounding_budget(q, k, v, do, causal: bool, scale: float, L, D, threads: int = 0,
+                             lib=None) -> dict:
+    """The sums that bound the rounding of P and dS to 8 bits in a backward
+    pass (plain masks), from the forward statistics L, D of
+    ``attention_forward_backward``: vP[j] = sum_i P_ij^2 dO_i^2,
+    vK[j] = sum_i dS_ij^2 q_i^2, vQ[i] = sum_j dS_ij^2 k_j^2 (elementwise over
+    the head dim, [B,H,N,d]), nvis[j] = the query rows that see key j
+    ([B,H,N]), and dsmax = max |dS| per head ([B,H])."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    L, D = _f64(L), _f64(D)
+    B, H, N, d = q.shape
+    out = {name: np.zeros_like(q) for name in ("vP", "vK", "vQ")}
+    out["nvis"] = np.zeros((B, H, N))
+    out["dsmax"] = np.zeros((B, H))
+    st = (lib or load()).oracle_attn_bwd_budget(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L), _ptr(D), B * H, N, d, int(bool(causal)),
+        float(scale), _ptr(out["vP"]), _ptr(out["vK"]), _ptr(out["vQ"]), _ptr(out["nvis"]),
+        _ptr(out["dsmax"]), int(threads))
+    if st != 0:
+        raise RuntimeError("oracle_attn_bwd_budget failed with status %d" % st)
     return out

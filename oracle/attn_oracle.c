@@ -396,3 +396,81 @@ int oracle_attn_head_rows(const double *Q, const double *K, const double *V,
   free(O); free(L); free(D);
   return st;
 }
+
+/* Rounding budget of a backward whose P and dS are rounded to 8 bits.
+ *
+ * For the fp8 backward the test needs, per output element, the sums that
+ * the rounding errors of P and dS are multiplied by:
+ *   vP[j][c]  = sum_i P_ij^2 dO_ic^2      (dV_jc = sum_i P_ij dO_ic)
+ *   vK[j][c]  = sum_i dS_ij^2 q_ic^2      (dK_jc = s sum_i dS_ij q_ic)
+ *   vQ[i][c]  = sum_j dS_ij^2 k_jc^2      (dQ_ic = s sum_j dS_ij k_jc)
+ *   nvis[j]   = number of query rows that see key j (for the absolute error
+ *               of values below the 8-bit format's normal range)
+ * and the largest |dS_ij| of each head, dsmax[h].  P and dS are the same
+ * quantities as in the backward above (plain masks: causal or none), from
+ * the L and D that oracle_attn_fwd_bwd returned. */
+static void budget_query_row(const double *Qh, const double *Kh, const double *Vh,
+                             const double *dOh, double Lrow, double Drow, long N, long d,
+                             int causal, double scale, long i, double *vQi, double *dsmax_row) {
+  const double *qrow = Qh + i * d, *dorow = dOh + i * d;
+  const long nk = causal ? i + 1 : N;
+  double mx = 0.0;
+  for (long c = 0; c < d; ++c) vQi[c] = 0.0;
+  for (long j = 0; j < nk; ++j) {
+    const double prob = exp(scale * dot(qrow, Kh + j * d, d) - Lrow);
+    const double dsv = prob * (dot(dorow, Vh + j * d, d) - Drow);
+    const double *krow = Kh + j * d;
+    for (long c = 0; c < d; ++c) vQi[c] += dsv * dsv * krow[c] * krow[c];
+    if (fabs(dsv) > mx) mx = fabs(dsv);
+  }
+  *dsmax_row = mx;
+}
+
+static void budget_key_row(const double *Qh, const double *Kh, const double *Vh,
+                           const double *dOh, const double *Lh, const double *Dh, long N,
+                           long d, int causal, double scale, long j, double *vPj, double *vKj,
+                           double *nvis) {
+  const double *krow = Kh + j * d, *vrow = Vh + j * d;
+  for (long c = 0; c < d; ++c) vPj[c] = vKj[c] = 0.0;
+  const long first = causal ? j : 0;
+  for (long i = first; i < N; ++i) {
+    const double *qrow = Qh + i * d, *dorow = dOh + i * d;
+    const double prob = exp(scale * dot(qrow, krow, d) - Lh[i]);
+    const double dsv = prob * (dot(dorow, vrow, d) - Dh[i]);
+    for (long c = 0; c < d; ++c) {
+      vPj[c] += prob * prob * dorow[c] * dorow[c];
+      vKj[c] += dsv * dsv * qrow[c] * qrow[c];
+    }
+  }
+  *nvis = (double)(N - first);
+}
+
+int oracle_attn_bwd_budget(const double *Q, const double *K, const double *V, const double *dO,
+                           const double *L, const double *D, long BH, long N, long d,
+                           int causal, double scale, double *vP, double *vK, double *vQ,
+                           double *nvis, double *dsmax, int nthreads) {
+  if (BH < 0 || N < 0 || d < 0) return ORACLE_ERR_ARG;
+  if (BH * N == 0) return ORACLE_OK;
+  if (!Q || !K || !V || !dO || !L || !D || !vP || !vK || !vQ || !nvis || !dsmax)
+    return ORACLE_ERR_ARG;
+  set_threads(nthreads);
+  double *rowmax = (double *)malloc(sizeof(double) * (size_t)(BH * N));
+  if (!rowmax) return ORACLE_ERR_NOMEM;
+#pragma omp parallel for collapse(2) schedule(dynamic, 16)
+  for (long h = 0; h < BH; ++h)
+    for (long r = 0; r < N; ++r) {
+      const double *Qh = Q + h * N * d, *Kh = K + h * N * d, *Vh = V + h * N * d;
+      const double *dOh = dO + h * N * d;
+      budget_query_row(Qh, Kh, Vh, dOh, L[h * N + r], D[h * N + r], N, d, causal, scale, r,
+                       vQ + (h * N + r) * d, rowmax + h * N + r);
+      budget_key_row(Qh, Kh, Vh, dOh, L + h * N, D + h * N, N, d, causal, scale, r,
+                     vP + (h * N + r) * d, vK + (h * N + r) * d, nvis + h * N + r);
+    }
+  for (long h = 0; h < BH; ++h) {
+    double m = 0.0;
+    for (long r = 0; r < N; ++r) m = rowmax[h * N + r] > m ? rowmax[h * N + r] : m;
+    dsmax[h] = m;
+  }
+  free(rowmax);
+  return ORACLE_OK;
+}

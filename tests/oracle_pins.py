@@ -567,6 +567,35 @@ def pin_e4m3_decoder(lib):
     assert np.all(both_nan | (ref == got))
 
 
+def pin_rounding_budget_brute_force(lib):
+    """The rounding-budget sums of the 8-bit backward against full N x N
+    matrices built in numpy (P, dP, dS written out from the definition)."""
+    rng = np.random.default_rng(29)
+    for causal in (False, True):
+        B, H, N, d = 1, 2, 9, 4
+        q, k, v, do = (_rand(rng, (B, H, N, d)) for _ in range(4))
+        s = 0.41
+        ref = _fb(lib, q, k, v, do, causal, s)
+        got = oracle.backward_rounding_budget(q, k, v, do, causal, s, ref["L"], ref["D"],
+                                              lib=lib)
+        for h in range(H):
+            S = s * q[0, h] @ k[0, h].T
+            if causal:
+                S = np.where(np.tril(np.ones((N, N), bool)), S, -np.inf)
+            m = S.max(axis=1, keepdims=True)
+            P = np.exp(S - m)
+            P /= P.sum(axis=1, keepdims=True)
+            O = P @ v[0, h]
+            Dv = np.sum(do[0, h] * O, axis=1)
+            dS = P * (do[0, h] @ v[0, h].T - Dv[:, None])
+            _close(got["vP"][0, h], (P ** 2).T @ do[0, h] ** 2, 1e-12, what="budget vP")
+            _close(got["vK"][0, h], (dS ** 2).T @ q[0, h] ** 2, 1e-12, what="budget vK")
+            _close(got["vQ"][0, h], (dS ** 2) @ k[0, h] ** 2, 1e-12, what="budget vQ")
+            vis = np.tril(np.ones((N, N))) if causal else np.ones((N, N))
+            assert np.array_equal(got["nvis"][0, h], vis.sum(axis=0))
+            _close(got["dsmax"][0, h], np.abs(dS).max(), 1e-12, what="budget dsmax")
+
+
 ALL_PINS = [
     pin_finite_differences,
     pin_single_key,
@@ -588,4 +617,5 @@ ALL_PINS = [
     pin_doc_brute_force,
     pin_doc_torch_fp64,
     pin_e4m3_decoder,
+    pin_rounding_budget_brute_force,
 ]

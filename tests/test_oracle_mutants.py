@@ -33,6 +33,10 @@ MUTANTS = {
                                   "const Mask mk = {causal, window, NULL};"),
     "sampler_ignores_window": ("const Mask mk = {causal, window, doc};",
                                "const Mask mk = {causal, 0, doc};"),
+    "budget_vk_uses_k": ("vKj[c] += dsv * dsv * qrow[c] * qrow[c];",
+                         "vKj[c] += dsv * dsv * krow[c] * krow[c];"),
+    "budget_vp_not_squared": ("vPj[c] += prob * prob * dorow[c] * dorow[c];",
+                              "vPj[c] += prob * dorow[c] * dorow[c];"),
     "D_uses_wrong_row": ("if (dOh && Di_out) *Di_out = dot(dOh + i * d, Oi, d);",
                          "if (dOh && Di_out) *Di_out = dot(dOh + (N - 1 - i) * d, Oi, d);"),
 }
