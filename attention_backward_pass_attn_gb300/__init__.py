@@ -10,7 +10,7 @@ library; the first call into ``binding`` does, and raises if it is missing.
 from .inputs import WORKLOADS, WORKLOAD_ORDER, Workload, make_inputs  # noqa: F401
 
 _BINDING_NAMES = (
-    "attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main",
+    "attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_fp8", "attn_bwd_preprocess", "attn_bwd_main",
     "attn_bwd_dq_convert", "attn_bwd_main_dkdv", "attn_bwd_dq", "attn_bwd_workspace_size", "alloc_workspace",
     "attn_last_device_error", "attn_device_error_word", "attn_watchdog_selftest",
     "status_string", "AttnError", "load_library", "ssd_fwd", "ssd_bwd", "ssd_workspace", "ATTN_DQ_AUTO", "ATTN_DQ_REDUCE",

@@ -65,6 +65,8 @@ def load_library(path: str | None = None):
             "attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
             "attn_bwd_ex": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f, vp,
                                 sz, vp]),
+            "attn_bwd_fp8": (i, [vp, vp, vp, vp, vp, vp, f, f, f, f, f, vp, vp, vp, vp, i, i, i,
+                                 i, i, f, vp, sz, vp]),
             "attn_bwd_opts": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, f,
                                   i, vp, sz, vp]),
             "attn_bwd_main_dkdv": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
@@ -208,6 +210,41 @@ def attn_fwd_fp8(q8, k8, v8, descales, causal: bool, scale=None, out=None, lse=N
                                      _stream(stream))
     _check("attn_fwd_fp8", st)
     return out, lse
+
+
+def attn_bwd_fp8(q8, k8, v8, o, do8, lse, descales, ds_scale: float, causal: bool, scale=None,
+                 ds_amax=None, workspace=None, stream=None):
+    """dQ, dK, dV (bf16) of exact attention with e4m3 operands.
+
+    q8, k8, v8, do8: e4m3 bytes [B, H, N, 128]; descales: (q, k, v, dO)
+    factors; o (bf16) and lse: the forward's outputs; ds_scale: the factor
+    dS is multiplied by before its rounding to e4m3 (keep ds_scale x
+    max|dS| <= 448).  ds_amax: a 1-element float32 CUDA tensor that receives
+    the largest |dS| of the call (or None).  Returns (dQ, dK, dV).
+    """
+    B, H, N, d = _shape4(q8, "q8")
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8"), (do8, "do8")):
+        _check_fp8(t, n, (B, H, N, d))
+    _check_tensor(o, "o", (B, H, N, d))
+    _check_tensor(lse, "lse", (B, H, N), torch.float32)
+    if ds_amax is not None:
+        _check_tensor(ds_amax, "ds_amax", (1,), torch.float32)
+    dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+                  for _ in range(3))
+    if workspace is None:
+        workspace = alloc_workspace(B, H, N, d, q8.device)
+    qd, kd, vd, dod = (float(x) for x in descales)
+    st = load_library().attn_bwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(),
+                                     do8.data_ptr(), lse.data_ptr(), qd, kd, vd, dod,
+                                     float(ds_scale), dq.data_ptr(), dk.data_ptr(),
+                                     dv.data_ptr(),
+                                     None if ds_amax is None else ds_amax.data_ptr(), B, H, N,
+                                     d, int(bool(causal)), _default_scale(d, scale),
+                                     workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
+    _check("attn_bwd_fp8", st)
+    return dq, dk, dv
 
 
 def attn_bwd(q, k, v, o, do, lse, causal: bool, scale=None, dq=None, dk=None, dv=None,

@@ -333,6 +333,49 @@ int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_descale
       launch_fwd_fp8(mq, mk, mv, O, L, s, score_log2, v_descale, err, (cudaStream_t)stream));
 }
 
+int attn_bwd_fp8(const void* Q8, const void* K8, const void* V8, const void* O, const void* dO8,
+                 const float* L, float q_descale, float k_descale, float v_descale,
+                 float do_descale, float ds_scale, void* dQ, void* dK, void* dV, float* ds_amax,
+                 int B, int H, int N, int d, int causal, float scale, void* workspace,
+                 size_t workspace_bytes_, void* stream) {
+  Shape s;
+  bool empty = false;
+  int st = make_shape(B, H, N, d, causal, &s, &empty);
+  if (st != ATTN_OK) return st;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  for (float f : {scale, q_descale, k_descale, v_descale, do_descale, ds_scale})
+    if (!scale_ok(f)) return ATTN_ERR_INVALID_ARG;
+  Fp8BwdScales sc;
+  sc.score_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  sc.dp_mult = v_descale * do_descale;
+  sc.ds_scale = ds_scale;
+  sc.dk_mult = scale * q_descale / ds_scale;
+  sc.dv_mult = do_descale / 256.f;
+  const float dq_mult = scale * k_descale / ds_scale;
+  for (float f : {sc.score_log2, sc.dp_mult, sc.dk_mult, sc.dv_mult, dq_mult})
+    if (!scale_ok(f)) return ATTN_ERR_INVALID_ARG;
+  if (ds_amax && (reinterpret_cast<uintptr_t>(ds_amax) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (empty) return ATTN_OK;
+  if ((st = check_ptrs({Q8, K8, V8, O, dO8, L, dQ, dK, dV})) != ATTN_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes_, s)) != ATTN_OK) return st;
+  int* err = error_word_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  const Workspace ws = carve_workspace(workspace, s);
+  CUtensorMap mq, mk, mv, mdo, macc;
+  if (make_tile_map_u8(&mq, Q8, s) || make_tile_map_u8(&mk, K8, s) ||
+      make_tile_map_u8(&mv, V8, s) || make_tile_map_u8(&mdo, dO8, s) ||
+      make_acc_map(&macc, ws.acc, s))
+    return ATTN_ERR_CUDA;
+  cudaStream_t strm = (cudaStream_t)stream;
+  if ((st = cuda_status(launch_bwd_fp8_preprocess(O, dO8, L, ws, s, do_descale, ds_amax,
+                                                  strm))) != ATTN_OK)
+    return st;
+  if ((st = cuda_status(launch_bwd_fp8_main(mq, mk, mv, mdo, macc, dK, dV, ws, s, sc, ds_amax,
+                                            err, strm))) != ATTN_OK)
+    return st;
+  return cuda_status(launch_bwd_dq_convert(dQ, ws, s, dq_mult, strm));
+}
+
 int attn_bwd_preprocess(const void* O, const void* dO, const float* L, int B, int H, int N, int d,
                         void* workspace, size_t workspace_bytes_, void* stream) {
   Shape s;

@@ -114,6 +114,21 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, void* O, float* L, const Shape& s,
                            float score_log2, float v_descale, int* err, cudaStream_t stream);
 
+// Factors of the e4m3 backward (attn_bwd_fp8.cu): the score scale
+// s qd kd log2(e), dP's scale vd dod, the caller's dS quantisation scale,
+// and the output factors of dK (s qd / ds_scale) and dV (dod / 256).
+struct Fp8BwdScales {
+  float score_log2, dp_mult, ds_scale, dk_mult, dv_mult;
+};
+cudaError_t launch_bwd_fp8_preprocess(const void* O, const void* dO8, const float* L,
+                                      const Workspace& ws, const Shape& s, float do_descale,
+                                      float* ds_amax, cudaStream_t stream);
+cudaError_t launch_bwd_fp8_main(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                const CUtensorMap& tmAcc, void* dK, void* dV, const Workspace& ws,
+                                const Shape& s, const Fp8BwdScales& sc, float* ds_amax, int* err,
+                                cudaStream_t stream);
+
 cudaError_t launch_bwd_preprocess(const void* O, const void* dO, const float* L,
                                   const Workspace& ws, const Shape& s, bool zero_acc,
                                   cudaStream_t stream);

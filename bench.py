@@ -411,6 +411,45 @@ def ssd_chunked_flops(w, chunk: int = 64):
     return float(per) * w.Bt * w.H * nc
 
 
+def time_fp8_backward(w, steps: int, warmup: int, flush):
+    """attn_bwd_fp8 on the workload's inputs quantised to e4m3 (per-tensor
+    descales), O and L from attn_fwd_fp8, dS scaled the way fp8 training
+    scales it (a first call reports max |dS|; the timed calls use the largest
+    power of two that keeps it within e4m3's range); per-call CUDA-event
+    times (ms)."""
+    import torch
+
+    from attention_backward_pass_attn_gb300 import binding as ab
+    from attention_backward_pass_attn_gb300.inputs import make_inputs, quantize_e4m3
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, do = make_inputs(w)
+    (q8, qd), (k8, kd), (v8, vd), (do8, dod) = (quantize_e4m3(t) for t in (q, k, v, do))
+    q8, k8, v8, do8 = (t.to(dev) for t in (q8, k8, v8, do8))
+    o, lse = ab.attn_fwd_fp8(q8, k8, v8, (qd, kd, vd), w.causal, w.scale)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    ws = ab.alloc_workspace(w.B, w.H, w.N, w.d, dev)
+    ab.attn_bwd_fp8(q8, k8, v8, o, do8, lse, (qd, kd, vd, dod), 1.0, w.causal, w.scale,
+                    ds_amax=amax, workspace=ws)
+    torch.cuda.synchronize()
+    ds_scale = 2.0 ** math.floor(math.log2(448.0 / max(float(amax.item()), 1e-30)))
+    stream = torch.cuda.current_stream()
+    rec = []
+    for i in range(warmup + steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ab.attn_bwd_fp8(q8, k8, v8, o, do8, lse, (qd, kd, vd, dod), ds_scale, w.causal, w.scale,
+                        ds_amax=amax, workspace=ws, stream=stream)
+        e1.record(stream)
+        if i >= warmup:
+            rec.append((e0, e1))
+    torch.cuda.synchronize()
+    if ab.attn_last_device_error() != ab.ATTN_OK:
+        raise RuntimeError("device error during the fp8 backward")
+    return [a.elapsed_time(b) for a, b in rec]
+
+
 def e2e_workload(w, steps: int, warmup: int):
     """The step through the public API with pinned host buffers, pipelined as a
     training loop would run it: each step copies its inputs host -> device,
@@ -626,13 +665,21 @@ def run_ours(args):
         for name in [n for n in [w.name] + OTHER if WORKLOADS[n].d == 128]:
             fw = WORKLOADS[name]
             ms = statistics.median(time_fp8_forward(fw, 10, 3, flush))
-            bf = statistics.median(time_workload(fw, 10, 3, flush)["fwd"])
+            bms = statistics.median(time_fp8_backward(fw, 10, 3, flush))
+            bf = time_workload(fw, 10, 3, flush)
             f8[name] = {"fp8_fwd_ms": round(ms, 4),
                         "fp8_fwd_tflops": round(fw.fwd_flops() / ms / 1e9, 1),
                         "fp8_fwd_frac_of_fp8_peak": round(fw.fwd_flops() / ms / 1e9
                                                           / (2 * peak_tf), 4),
-                        "bf16_fwd_tflops": round(fw.fwd_flops() / bf / 1e9, 1)}
-        extra["fp8_forward"] = {"peak_tflops": 2 * peak_tf,
+                        "bf16_fwd_tflops": round(fw.fwd_flops() / statistics.median(bf["fwd"])
+                                                 / 1e9, 1),
+                        "fp8_bwd_ms": round(bms, 4),
+                        "fp8_bwd_tflops": round(fw.bwd_flops() / bms / 1e9, 1),
+                        "fp8_bwd_frac_of_fp8_peak": round(fw.bwd_flops() / bms / 1e9
+                                                          / (2 * peak_tf), 4),
+                        "bf16_bwd_tflops": round(fw.bwd_flops() / statistics.median(bf["bwd"])
+                                                 / 1e9, 1)}
+        extra["fp8"] = {"peak_tflops": 2 * peak_tf,
                                 "peak_source": "measured bf16_tflops x 2 (nominal fp8/bf16 "
                                                "dense ratio 4.5/2.25)",
                                 "workloads": f8}
@@ -765,6 +812,10 @@ def run_leg(args):
         return {"leg": "ssd", "workload": w.name, "fwd_ms": statistics.median(f_ms),
                 "bwd_ms": statistics.median(b_ms)}
     w = workload_of(args)
+    if args.leg == "fp8_backward":
+        ms = statistics.median(time_fp8_backward(w, steps, warm, flush))
+        return {"leg": "fp8_backward", "workload": w.name, "ms": ms,
+                "tflops": w.bwd_flops() / ms / 1e9}
     if args.leg == "fp8_forward":
         ms = statistics.median(time_fp8_forward(w, steps, warm, flush))
         return {"leg": "fp8_forward", "workload": w.name, "ms": ms,
@@ -852,7 +903,7 @@ def main(argv=None):
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--leg", default="attention",
-                   choices=["attention", "fp8_forward", "dq_separate", "ssd"],
+                   choices=["attention", "fp8_forward", "fp8_backward", "dq_separate", "ssd"],
                    help="run one other leg alone on --workload (for profiler captures); "
                         "prints its timing, not the benchmark line")
     args = p.parse_args(argv)

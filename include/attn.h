@@ -116,6 +116,29 @@ int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, float q_descale
                  int causal, float scale, void* stream);
 
 /*
+ * Backward with 8-bit floating-point operands, the fp8 extension of the same
+ * page section "Summary" applied to the backward: all five contractions per
+ * tile pair (S^T, dP^T, dV, dK, dQ) run on e4m3 operands on the tensor core
+ * with fp32 accumulation.  Q8, K8, V8, dO8: E4M3 bytes [B][H][N][d] standing
+ * for byte x q_descale (k_descale, v_descale, do_descale); O: the forward's
+ * output, bf16; L: its log-sum-exp.  Writes dQ, dK, dV (bf16) as attn_bwd
+ * does, with the same workspace (attn_bwd_workspace_size).
+ *
+ * The probabilities are rounded to e4m3 as 256 P (P <= 1); dS = P o (dP - D)
+ * is rounded as ds_scale x dS, where ds_scale is the caller's: the largest
+ * |dS| the call met is stored in *ds_amax (a device float; NULL = not
+ * reported), so the caller can pick the next call's scale with
+ * ds_scale x amax <= 448 (delayed scaling).  Values of ds_scale x dS beyond
+ * 448 saturate.  d must be 128 (ATTN_ERR_UNSUPPORTED otherwise); the causal
+ * mask or none; every factor finite and > 0.
+ */
+int attn_bwd_fp8(const void* Q8, const void* K8, const void* V8, const void* O, const void* dO8,
+                 const float* L, float q_descale, float k_descale, float v_descale,
+                 float do_descale, float ds_scale, void* dQ, void* dK, void* dV, float* ds_amax,
+                 int B, int H, int N, int d, int causal, float scale, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/*
  * Interface utility of this library's boundary; the paper has no counterpart.
  * Bytes of device workspace attn_bwd needs for this shape (0 for an empty
  * problem).  Holds, per head, D = rowsum(dO o O) and L scaled to base 2, each

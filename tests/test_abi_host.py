@@ -198,6 +198,27 @@ def test_ssd_validation(lib):
                        ws_need, None) == ab.ATTN_ERR_INVALID_ARG
 
 
+def test_fp8_backward_validation(lib):
+    """attn_bwd_fp8: head dim 128 only, every factor finite and > 0, pointers,
+    workspace and the amax word checked before any launch."""
+    need = lib.attn_bwd_workspace_size(1, 2, 128, 128)
+
+    def b8(d=128, N=128, ptr=FAKE, ds=1.0, qd=1.0, amax=None, ws=FAKE, wsb=None, causal=1):
+        return lib.attn_bwd_fp8(ptr, ptr, ptr, ptr, ptr, ptr, qd, 1.0, 1.0, 1.0, ds, ptr, ptr, ptr,
+                                amax, 1, 2, N, d, causal, 0.088, ws, need if wsb is None else wsb,
+                                None)
+    assert b8(d=64) == ab.ATTN_ERR_UNSUPPORTED
+    assert b8(ds=0.0) == ab.ATTN_ERR_INVALID_ARG
+    assert b8(ds=float("nan")) == ab.ATTN_ERR_INVALID_ARG
+    assert b8(qd=-1.0) == ab.ATTN_ERR_INVALID_ARG
+    assert b8(amax=FAKE + 2) == ab.ATTN_ERR_INVALID_ARG
+    assert b8(ptr=None) == ab.ATTN_ERR_INVALID_ARG
+    assert b8(ws=None) == ab.ATTN_ERR_WORKSPACE
+    assert b8(wsb=need - 1) == ab.ATTN_ERR_WORKSPACE
+    assert b8(causal=2) == ab.ATTN_ERR_INVALID_ARG
+    assert b8(ptr=None, N=0, ws=None, wsb=0) == ab.ATTN_OK
+
+
 def test_noalloc_passes_argument_errors_through(lib):
     """attn_bwd_noalloc answers every bad argument the way attn_bwd does, before
     it looks up its scratch (nothing here reaches the GPU): an unsupported head
