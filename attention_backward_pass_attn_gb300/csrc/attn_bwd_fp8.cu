@@ -367,6 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
           tmem_wait_ld();
           const bool diag = CAUSAL && qt == jt;
+          // key rows past N (the zero-filled tail of the last tile) get P = 0:
+          // their K and V rows are zero, and 2^(-L) must not reach dS
+          const bool dead_key = jt * 128 + r >= N;
           uint32_t p8[16];
           const float4* L2v4 = reinterpret_cast<const float4*>(L2v);
 #pragma unroll
@@ -376,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), score_log2, -l.y));
             float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), score_log2, -l.z));
             float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), score_log2, -l.w));
+            if (dead_key) p0 = p1 = p2 = p3 = 0.f;
             if (diag) {  // key row r is visible to query columns >= r only
               const int q0 = 64 * h + 4 * c4;
               if (q0 < r) p0 = 0.f;

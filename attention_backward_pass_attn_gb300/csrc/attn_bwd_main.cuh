@@ -503,6 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
           tmem_wait_ld();
           const bool diag = CAUSAL && qt == jt;
+          // key rows past N (the zero-filled tail of the last tile) get P = 0:
+          // their K and V rows are zero, and 2^(-L) must not reach dS
+          const bool dead_key = jt * 128 + r >= N;
           // sliding window: query column q of this tile sees key row r only
           // while (qt - jt) * 128 + q - r < window
           const int dq_tile = (qt - jt) * 128;
@@ -518,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), scale_log2, -l.y));
             float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), scale_log2, -l.z));
             float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), scale_log2, -l.w));
+            if (dead_key) p0 = p1 = p2 = p3 = 0.f;
             if (diag) {  // key row r is visible to query columns >= r only
               const int q0 = 64 * h + 4 * c4;
               if (q0 < r) p0 = 0.f;

@@ -73,20 +73,22 @@ def run_case(q, k, v, do, causal, what):
                     1.0, causal, s, ds_amax=amax)
     torch.cuda.synchronize()
     m = float(amax.item())
-    assert m > 0 and math.isfinite(m), "ds_amax %r" % m
-    ds_scale = 2.0 ** math.floor(math.log2(448.0 / m))
+    assert m >= 0 and math.isfinite(m), "ds_amax %r" % m
+    ds_scale = 2.0 ** math.floor(math.log2(448.0 / m)) if m > 0 else 1.0
     dq, dk, dv = ab.attn_bwd_fp8(args[0], args[1], args[2], args[3], args[4], args[5],
                                  (qd, kd, vd, dod), ds_scale, causal, s, ds_amax=amax)
     torch.cuda.synchronize()
     st, word = ab.attn_device_error_word()
     assert st == ab.ATTN_OK, "device error %d word 0x%08x" % (st, word)
-    # the reported maximum agrees with the oracle's max |dS| (rounding aside)
-    budget = oracle.backward_rounding_budget(qf, kf, vf, dof, causal, s, ref["L"], ref["D"])
-    dsmax = float(np.max(budget["dsmax"]))
-    assert abs(float(amax.item()) - dsmax) <= 0.02 * dsmax, (amax.item(), dsmax)
     # the D term: dD_i <= 2^-9 sum_c |dO_ic O_ic|
     o_used = o_bf.to(torch.float64).numpy()
     dD = 2.0 ** -9 * np.sum(np.abs(dof * o_used), axis=-1)                # [B,H,N]
+    # the reported maximum agrees with the oracle's max |dS| up to P's bf16
+    # rounding (2^-8 relative, with a margin) and the D term (|P| <= 1)
+    budget = oracle.backward_rounding_budget(qf, kf, vf, dof, causal, s, ref["L"], ref["D"])
+    dsmax = float(np.max(budget["dsmax"]))
+    assert abs(float(amax.item()) - dsmax) <= 0.02 * dsmax + float(np.max(dD)), \
+        (amax.item(), dsmax)
     wK = oracle.attention_forward_backward(qf, kf, vf, dD[..., None] * np.abs(qf), causal,
                                            s)["dV"] * s   # sum_i P_ij |dD_i| |q_ic|
     wQ = s * dD[..., None] * oracle.attention_forward(qf, kf, np.abs(kf), causal, s)[0]
