@@ -379,7 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), score_log2, -l.y));
             float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), score_log2, -l.z));
             float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), score_log2, -l.w));
-            if (dead_key) p0 = p1 = p2 = p3 = 0.f;
             if (diag) {  // key row r is visible to query columns >= r only
               const int q0 = 64 * h + 4 * c4;
               if (q0 < r) p0 = 0.f;
@@ -390,6 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[2 * c4] = pack_bf16x2(p0, p1);
             pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
             p8[c4] = pack_e4m3x4(p0 * kPScale, p1 * kPScale, p2 * kPScale, p3 * kPScale);
+          }
+          if (dead_key) {  // only in the last, ragged key tile
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) p8[c] = 0u;
           }
           tmem_st16(tS, p8);
           tmem_wait_st();

@@ -521,7 +521,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), scale_log2, -l.y));
             float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), scale_log2, -l.z));
             float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), scale_log2, -l.w));
-            if (dead_key) p0 = p1 = p2 = p3 = 0.f;
             if (diag) {  // key row r is visible to query columns >= r only
               const int q0 = 64 * h + 4 * c4;
               if (q0 < r) p0 = 0.f;
@@ -545,6 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[2 * c4] = pack_bf16x2(p0, p1);
             pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
+          }
+          if (dead_key) {  // only in the last, ragged key tile
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = 0u;
           }
           tmem_st32(tS, pk);
           tmem_wait_st();
