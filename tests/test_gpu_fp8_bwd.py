@@ -111,7 +111,7 @@ def run_case(q, k, v, do, causal, what):
         worst = float(np.max(err / bound))
         rms = float(np.sqrt(np.mean(err ** 2)))
         rms_pred = float(np.sqrt(np.mean(var + (2.0 ** -9 * r) ** 2 + np.square(w))))
-        rel = float(np.max(err) / rmax)
+        rel = float(np.max(err) / rmax) if rmax > 0 else float(np.max(err))
         msg = "%s %s: worst err/bound %.3f, rms %.3e (predicted %.3e), max|err|/max %.3e" % (
             what, name, worst, rms, rms_pred, rel)
         assert worst <= 1.0, msg
