@@ -107,6 +107,7 @@ KERNEL_SOURCES = {
     "attn_bwd_dq_convert_kernel": ["attn_bwd.cu", "attn_bwd_main.cuh", "ptx.cuh", "mask.cuh"],
     "attn_fwd_kernel": ["attn_fwd.cu", "ptx.cuh", "mask.cuh"],
     "attn_fwd_fp8_kernel": ["attn_fwd_fp8.cu", "ptx.cuh"],
+    "attn_bwd_fp8_kernel": ["attn_bwd_fp8.cu", "ptx.cuh"],
     "ssd_chunk_bwd_kernel": ["ssd.cu", "ptx.cuh"],
 }
 
