@@ -12,16 +12,19 @@
 // with both contractions in fp8 and fp32 accumulation.  P is quantised to
 // e4m3 for P V; the row sums and L use the unquantised fp32 probabilities.
 //
-// Design: the bf16 forward's (attn_fwd.cu) -- one CTA owns two 128-row query
-// tiles of one head, K/V tiles stream through a two-stage TMA ring, warps 0-3
-// and 4-7 run the softmax of the two tiles, warp 8 issues TMA, warp 9 issues
-// tcgen05.mma -- with 8-bit operands: a 128 x 128 e4m3 tile is one
+// Design: the bf16 forward's (attn_fwd.cu) -- CTAs taking tasks of two
+// 128-row query tiles of one head in turn (heaviest first under the causal
+// mask; the grid from fwd_grid), K/V tiles streaming through a two-stage TMA
+// ring that runs on across a CTA's tasks, warps 0-3 and 4-7 running the
+// softmax of the two tiles, warp 8 issuing TMA, warp 9 issuing tcgen05.mma --
+// with 8-bit operands: a 128 x 128 e4m3 tile is one
 // 128-byte-swizzled block of 16 KB (head dim 128 only), an MMA takes K = 32,
 // and P goes to tensor memory four e4m3 values per 32-bit column.  The row
 // maximum is exact (no lazy threshold): P is formed as 2^(x - m + 8), at most
 // 256, so that e4m3's normal range (down to 2^-6) covers probabilities down
 // to 2^-14 of the row maximum.
 
+#include "f32x2.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -38,14 +41,15 @@ constexpr int kTileBytes = 128 * HD;  // one 128-row e4m3 tile: 16 KB
 constexpr float kPShift = 8.f;    // P = 2^(x - m + 8) <= 256
 
 constexpr int kBarQFull = 0;
-constexpr int kBarKFull = 1;                       // + stage
+constexpr int kBarQEmpty = 1;
+constexpr int kBarKFull = 2;                       // + stage
 constexpr int kBarKEmpty = kBarKFull + kStages;    // + stage
 constexpr int kBarVFull = kBarKEmpty + kStages;    // + stage
 constexpr int kBarVEmpty = kBarVFull + kStages;    // + stage
 constexpr int kBarSFull = kBarVEmpty + kStages;    // + tile
 constexpr int kBarPReady = kBarSFull + 2;          // + tile
-constexpr int kBarOFull = kBarPReady + 2;
-constexpr int kBarDrain = kBarOFull + 1;
+constexpr int kBarOFull = kBarPReady + 2;          // + tile
+constexpr int kBarDrain = kBarOFull + 2;
 constexpr int kNumBars = kBarDrain + 1;
 
 struct Layout {
@@ -86,11 +90,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_tiles = (N + 127) >> 7;
   const int n_pairs = (n_tiles + 1) >> 1;
-  const int bh = CAUSAL ? int(blockIdx.x % BH) : int(blockIdx.x / n_pairs);
-  const int pair = CAUSAL ? (n_pairs - 1 - int(blockIdx.x / BH)) : int(blockIdx.x % n_pairs);
-  const int qt_a = 2 * pair;
-  const bool has_b = qt_a + 1 < n_tiles;
-  const int n_kv = CAUSAL ? min(n_tiles, qt_a + (has_b ? 2 : 1)) : n_tiles;
+  const int n_tasks = BH * n_pairs;
+  const int G = int(gridDim.x), cta = int(blockIdx.x);
+  // Task i: query tiles 2 pair and 2 pair + 1 of head bh against key/value
+  // tiles 0 .. n_kv - 1; causal tasks heaviest first, heads interleaved,
+  // else head by head.
+  struct Task {
+    int bh, qt_a, n_kv;
+    bool has_b;
+  };
+  auto task = [&](int i) {
+    Task t;
+    t.bh = CAUSAL ? i % BH : i / n_pairs;
+    t.qt_a = 2 * (CAUSAL ? n_pairs - 1 - i / BH : i % n_pairs);
+    t.has_b = t.qt_a + 1 < n_tiles;
+    t.n_kv = CAUSAL ? min(n_tiles, t.qt_a + (t.has_b ? 2 : 1)) : n_tiles;
+    return t;
+  };
+  // CTA b of G takes tasks b, 2G-1-b, 2G+b, ... (a snake over rounds); -1 past the end
+  auto snake = [&](int k) {
+    const long long idx = (k & 1) ? (long long)k * G + (G - 1 - cta) : (long long)k * G + cta;
+    return idx < n_tasks ? int(idx) : -1;
+  };
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kTmemSlot);
@@ -121,27 +142,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (elect_one()) {
-      mbar_arrive_expect_tx(bar(kBarQFull), (has_b ? 2 : 1) * kTileBytes);
-      for (int t = 0; t < (has_b ? 2 : 1); ++t)
-        tma_load_3d(sbase + Ly::kQ + t * kTileBytes, &tmQ, bar(kBarQFull), 0, (qt_a + t) * 128,
-                    bh);
-    }
-    __syncwarp();
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % kStages, n = j / kStages;
-      if (j >= kStages && !mbar_wait_warp(bar(kBarKEmpty + s), (n - 1) & 1, ctx, 0x410)) break;
+    // g counts key/value tiles across tasks; the query tiles of a task load
+    // once the previous task's last S has completed.
+    bool ok = true;
+    int g = 0;
+    for (int k = 0, i = snake(0); ok && i >= 0; i = snake(++k)) {
+      const Task tk = task(i);
+      if (k > 0 && !(ok = mbar_wait_warp(bar(kBarQEmpty), (k - 1) & 1, ctx, 0x412))) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-        tma_load_3d(sbase + Ly::kK + s * kTileBytes, &tmK, bar(kBarKFull + s), 0, j * 128, bh);
+        mbar_arrive_expect_tx(bar(kBarQFull), (tk.has_b ? 2 : 1) * kTileBytes);
+        for (int t = 0; t < (tk.has_b ? 2 : 1); ++t)
+          tma_load_3d(sbase + Ly::kQ + t * kTileBytes, &tmQ, bar(kBarQFull), 0,
+                      (tk.qt_a + t) * 128, tk.bh);
       }
       __syncwarp();
-      if (j >= kStages && !mbar_wait_warp(bar(kBarVEmpty + s), (n - 1) & 1, ctx, 0x411)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-        tma_load_3d(sbase + Ly::kV + s * kTileBytes, &tmV, bar(kBarVFull + s), 0, j * 128, bh);
+      for (int j = 0; j < tk.n_kv; ++j, ++g) {
+        const int s = g % kStages, n = g / kStages;
+        if (g >= kStages && !(ok = mbar_wait_warp(bar(kBarKEmpty + s), (n - 1) & 1, ctx, 0x410)))
+          break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
+          tma_load_3d(sbase + Ly::kK + s * kTileBytes, &tmK, bar(kBarKFull + s), 0, j * 128,
+                      tk.bh);
+        }
+        __syncwarp();
+        if (g >= kStages && !(ok = mbar_wait_warp(bar(kBarVEmpty + s), (n - 1) & 1, ctx, 0x411)))
+          break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
+          tma_load_3d(sbase + Ly::kV + s * kTileBytes, &tmV, bar(kBarVFull + s), 0, j * 128,
+                      tk.bh);
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -164,23 +197,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 4; ++k)  // 128 keys, 32 per step; P packed 4 per column
         mma_ts_f8(d, p + 8 * k, sdesc_add(dv, k * 4096), kIdO, k > 0 ? 1u : acc);
     };
-    bool ok = mbar_wait_warp(bar(kBarQFull), 0, ctx, 0x420) &&
-              mbar_wait_warp(bar(kBarKFull), 0, ctx, 0x421);
-    if (ok) {
+    // Handshake counts across tasks: g key/value tiles, ca (cb) S/P rounds of
+    // tile A (B).  A task's first P V overwrites O_t, which the softmax warps
+    // of tile t have read before they signal the first P of this task; the
+    // tensor core runs this thread's instructions in issue order, so an S
+    // written over P columns comes after the P V that reads them.
+    bool ok = true;
+    int g = 0, ca = 0, cb = 0;
+    for (int k = 0, i = snake(0); ok && i >= 0; i = snake(++k)) {
+      const Task tk = task(i);
+      const int n_kv = tk.n_kv;
+      if (!(ok = mbar_wait_warp(bar(kBarQFull), k & 1, ctx, 0x420))) break;
+      if (!(ok = mbar_wait_warp(bar(kBarKFull + g % kStages), (g / kStages) & 1, ctx, 0x421)))
+        break;
       tc_fence_after();
       if (elect_one()) {
-        issue_s(0, 0);
-        if (has_b) issue_s(1, 0);
-        tc_commit(bar(kBarKEmpty));
+        issue_s(0, g % kStages);
+        if (tk.has_b) issue_s(1, g % kStages);
+        if (n_kv == 1) tc_commit(bar(kBarQEmpty));  // the task's last S
+        tc_commit(bar(kBarKEmpty + g % kStages));
       }
       __syncwarp();
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % kStages;
+      for (int j = 0; j < n_kv; ++j, ++g) {
+        const int s = g % kStages;
         const bool next = j + 1 < n_kv;
-        const int s1 = (j + 1) % kStages, n1 = (j + 1) / kStages;
+        const int s1 = (g + 1) % kStages, n1 = (g + 1) / kStages;
         const uint32_t acc = j > 0 ? 1u : 0u;
-        if (!(ok = mbar_wait_warp(bar(kBarVFull + s), (j / kStages) & 1, ctx, 0x422))) break;
-        if (!(ok = mbar_wait_warp(bar(kBarPReady + 0), j & 1, ctx, 0x423))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarVFull + s), (g / kStages) & 1, ctx, 0x422))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarPReady + 0), (ca + j) & 1, ctx, 0x423))) break;
         tc_fence_after();
         if (elect_one()) issue_pv(0, s, acc);
         __syncwarp();
@@ -190,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (elect_one()) issue_s(0, s1);
           __syncwarp();
         }
-        if (has_b) {
-          if (!(ok = mbar_wait_warp(bar(kBarPReady + 1), j & 1, ctx, 0x425))) break;
+        if (tk.has_b) {
+          if (!(ok = mbar_wait_warp(bar(kBarPReady + 1), (cb + j) & 1, ctx, 0x425))) break;
           tc_fence_after();
           if (elect_one()) {
             issue_pv(1, s, acc);
@@ -200,13 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         if (elect_one()) {
+          if (j + 2 == n_kv) tc_commit(bar(kBarQEmpty));  // the task's last S was issued above
           tc_commit(bar(kBarVEmpty + s));
           if (next) tc_commit(bar(kBarKEmpty + s1));
         }
         __syncwarp();
       }
-      if (ok && elect_one()) tc_commit(bar(kBarOFull));
+      if (!ok) break;
+      if (elect_one()) {
+        tc_commit(bar(kBarOFull + 0));
+        if (tk.has_b) tc_commit(bar(kBarOFull + 1));
+      }
       __syncwarp();
+      ca += n_kv;
+      if (tk.has_b) cb += n_kv;
     }
     if (elect_one()) tc_commit(bar(kBarDrain));
     __syncwarp();
@@ -217,17 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;  // 0 = tile A, 1 = tile B
     const int r = threadIdx.x & 127;
-    if (t == 0 || has_b) {
-      const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-      const uint32_t tS = tbase + lane_off + Ly::kColS + 128 * t;
-      const uint32_t tO = tbase + lane_off + Ly::kColO + HD * t;
-      const int q_tile0 = (qt_a + t) * 128;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_off + Ly::kColS + 128 * t;
+    const uint32_t tO = tbase + lane_off + Ly::kColO + HD * t;
+    bool ok = true;
+    int cs = 0;  // S/P rounds of this tile so far
+    int no = 0;  // outputs of this tile so far
+    for (int k = 0, i = snake(0); ok && i >= 0; i = snake(++k)) {
+      const Task tk = task(i);
+      if (t == 1 && !tk.has_b) continue;
+      const int bh = tk.bh, n_kv = tk.n_kv;
+      const int q_tile0 = (tk.qt_a + t) * 128;
       const int q = q_tile0 + r;
       float m = -INFINITY;  // running (exact) max of the base-2 scaled scores
       float l = 0.f;        // running sum of 2^(x - m + 8), unquantised
-      bool ok = true;
       for (int j = 0; j < n_kv; ++j) {
-        if (!(ok = mbar_wait_warp(bar(kBarSFull + t), j & 1, ctx, 0x430 + t))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarSFull + t), (cs + j) & 1, ctx, 0x430 + t))) break;
         tc_fence_after();
         uint32_t u[128];
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
@@ -243,13 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((CAUSAL && kv > q) || kv >= N) u[c] = __float_as_uint(-INFINITY);
           }
         }
+        // row maximum: eight chains of three-input maxima (two scores each)
         float m8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(u[e]);
 #pragma unroll
-        for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(u[e]));
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int e = 8; e < 128; e += 2)
+          m8[(e >> 1) & 7] =
+              max3f(m8[(e >> 1) & 7], __uint_as_float(u[e]), __uint_as_float(u[e + 1]));
+        const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]),
+                               fmaxf(m8[6], m8[7]));
         const float m_new = fmaxf(m, mx * score_log2);  // score_log2 > 0
         const bool rescale = m_new > m;
         const float alpha = rescale ? ex2(m - m_new) : 1.f;
@@ -264,10 +323,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int c4 = 0; c4 < 32; ++c4) {
-          const float p0 = ex2(fmaf(__uint_as_float(u[4 * c4]), score_log2, -mb));
-          const float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), score_log2, -mb));
-          const float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), score_log2, -mb));
-          const float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), score_log2, -mb));
+          // s score_log2 - mb, two scores per instruction
+          float x0, x1, x2, x3;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(u[4 * c4]), __uint_as_float(u[4 * c4 + 1])),
+                                f32x2(score_log2, score_log2), f32x2(-mb, -mb)),
+                      x0, x1);
+          f32x2_split(
+              fma_f32x2(f32x2(__uint_as_float(u[4 * c4 + 2]), __uint_as_float(u[4 * c4 + 3])),
+                        f32x2(score_log2, score_log2), f32x2(-mb, -mb)),
+              x2, x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
           rs[c4 & 3] += (p0 + p1) + (p2 + p3);
           pk[c4] = pack_e4m3x4(p0, p1, p2, p3);
         }
@@ -291,7 +356,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(kBarPReady + t));
       }
-      if (ok && mbar_wait_warp(bar(kBarOFull), 0, ctx, 0x438 + t)) {
+      if (!ok) break;
+      cs += n_kv;
+      if (!(ok = mbar_wait_warp(bar(kBarOFull + t), no & 1, ctx, 0x438 + t))) break;
+      ++no;
+      {
         tc_fence_after();
         const float mult = v_descale / l;
         __nv_bfloat16* orow = O + (size_t(bh) * N + q) * HD;
@@ -338,8 +407,8 @@ static cudaError_t launch_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   auto kern = attn_fwd_fp8_kernel<CAUSAL>;
   cudaError_t e = set_smem_limit_once<attn_fwd_fp8_kernel<CAUSAL>>(Layout::kBytes);
   if (e != cudaSuccess) return e;
-  const int n_pairs = (s.n_tiles + 1) / 2;
-  const dim3 grid(unsigned(n_pairs) * unsigned(s.BH));
+  const long long n_tasks = (long long)((s.n_tiles + 1) / 2) * s.BH;
+  const dim3 grid(unsigned(fwd_grid(n_tasks, CAUSAL)));
   return launch_kernel(kern, grid, dim3(kThreads), Layout::kBytes, stream, tmQ, tmK, tmV,
                        reinterpret_cast<__nv_bfloat16*>(O), L, s.BH, s.N, score_log2, v_descale,
                        err);

@@ -47,6 +47,33 @@ struct Workspace {
   int* order;
 };
 
+// Streaming multiprocessors of the current device (cached per device).
+inline int device_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// Grid of the forward kernels over n_tasks tasks (query-tile pairs of one
+// head).  Without the causal mask every task costs the same: a persistent
+// grid, one CTA per SM taking its share of the tasks in turn, overlaps each
+// task's loads and first contraction with the previous one's tail.  Under
+// the mask tasks differ up to N/256-fold; with more than four per SM, one CTA
+// per task lets the hardware hand the next task to whichever SM frees first,
+// which balances the unequal tasks better than a fixed split (measured).
+inline long long fwd_grid(long long n_tasks, bool causal) {
+  const int sms = device_sm_count();
+  if (causal && n_tasks > 4LL * sms) return n_tasks;
+  return n_tasks < sms ? n_tasks : sms;
+}
+
 // Launches a kernel of this library with programmatic dependent launch
 // allowed: the kernel may start while the previous kernel in the stream is
 // finishing.  Every kernel of the library executes griddepcontrol.wait before

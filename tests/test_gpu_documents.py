@@ -144,3 +144,27 @@ def test_documents_long_sequence_sampled(method):
         msg = "head %d: %s L %.2e" % (h, errs, lerr)
         assert all(e <= TOL for e in errs.values()), msg
         assert lerr <= L_ATOL, msg
+
+
+def test_documents_many_batch_elements_forward():
+    """65 batch elements of N = 16384, each with its own packing (4160
+    query-tile pairs, one forward CTA each): sampled rows of O and L in the
+    first, a middle and the last batch element."""
+    B, H, N, d = 65, 1, 16384, 64
+    rng = np.random.default_rng(65)
+    docs = np.stack([doc_map(random_lengths(rng, N, 200, 3000)) for _ in range(B)])
+    q, k, v = (make_tensor((B, H, N, d), 6500 + i) for i in range(3))
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", 0)
+    dmap = torch.from_numpy(docs.astype(np.int32)).to(dev)
+    o, lse = ab.attn_fwd(q.to(dev), k.to(dev), v.to(dev), True, scale, doc=dmap)
+    torch.cuda.synchronize()
+    for b in (0, B // 2, B - 1):
+        starts = sorted(set(docs[b].tolist()))
+        rows = sorted(set([0, 127, 128, N - 1] + starts[:4] + [max(s - 1, 0) for s in starts[:4]]
+                          + rng.choice(N, 16, replace=False).tolist()))
+        ref = oracle.attention_head_rows(q[b, 0], k[b, 0], v[b, 0], q[b, 0], True, scale,
+                                         rows, [0], doc=docs[b])
+        err = rel_err(o[b, 0][rows], ref["O"])
+        lerr = float(np.max(np.abs(f64(lse[b, 0][rows]) - ref["L"])))
+        assert err <= TOL and lerr <= L_ATOL, "batch element %d: O %.2e L %.2e" % (b, err, lerr)

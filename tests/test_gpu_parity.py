@@ -157,6 +157,22 @@ def test_ragged_lengths(N, d, causal):
         check_full(gpu, ref, "N=%d d=%d causal=%s dq=%s" % (N, d, causal, mname))
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_tasks_per_cta_ragged(d, causal):
+    """More (head, query-tile pair) tasks than SMs but fewer than two per SM
+    (the forward's grid is then persistent with or without the causal mask),
+    half of them without a second query tile (N = 300: tiles of 128, 128 and
+    44 rows), so that forward CTAs run tasks of both kinds in turn."""
+    B, H, N = 2, 60, 300
+    seed = 5100 + d + int(causal)
+    q, k, v, do = (make_tensor((B, H, N, d), seed + 7919 * i) for i in range(4))
+    scale = 1.0 / math.sqrt(d)
+    ref = oracle.attention_forward_backward(q, k, v, do, causal, scale)
+    gpu = gpu_fwd_bwd(q, k, v, do, causal, scale)
+    check_full(gpu, ref, "B=%d H=%d N=%d d=%d causal=%s" % (B, H, N, d, causal))
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_zero_queries_uniform_softmax(d):
     """Q = 0: P is uniform over the visible keys; O is a (prefix) mean of V."""
