@@ -92,17 +92,6 @@ __device__ __forceinline__ int snake_item(int k, int b, int G, int n_items) {
   return idx < n_items ? idx : -1;
 }
 
-// 16 columns of 32-bit values to tensor memory (warp-collective).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
 // Descriptors: 128-byte swizzle, one 16 KB block per 128 x 128 e4m3 tile.
 // K-major: +32 bytes per 32-element k-step; MN-major: +4 KB (32 rows).
 

@@ -10,8 +10,9 @@
 //    P^T = 2^(S^T s log2e - L log2e)    softmax warps, written back as bf16
 //    dP^T = V dO^T            (tensor memory)
 //    dV  += P^T dO            (A operand read from tensor memory)
-//    dS^T = P^T o (dP^T - D)  softmax warps, bf16 into shared memory
-//    dK  += dS^T Q
+//    dS^T = P^T o (dP^T - D)  softmax warps, bf16 back into the dP^T
+//                             columns (and, for dQ, into shared memory)
+//    dK  += dS^T Q            (A operand read from tensor memory)
 //    dQ_i = dS K              (FUSED_DQ only: tensor memory, then staged
 //                              through shared memory and added into the fp32
 //                              accumulator by TMA reduce-add)
@@ -330,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dK_k = make_sdesc_sw128(sbase + Ly::kK, 16, 1024);        // K, K-major
     const uint64_t dK_mn = make_sdesc_sw128(sbase + Ly::kK, 16384, 1024);    // K, MN-major
     const uint64_t dV_k = make_sdesc_sw128(sbase + Ly::kV, 16, 1024);
-    const uint64_t dS_k = make_sdesc_sw128(sbase + Ly::kDS, 16, 1024);       // dS^T, K-major
     const uint64_t dS_mn = make_sdesc_sw128(sbase + Ly::kDS, 16384, 1024);   // dS, MN-major
     const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
     const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
@@ -349,8 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(bar(kBarSFull));
     };
-    // dK += dS^T Q, then dQ_i = dS K (into its own columns for d = 64, into
-    // the dP^T columns -- read by now -- for d = 128).
+    // dK += dS^T Q with dS^T read from the dP^T columns (packed there by the
+    // softmax warps), then dQ_i = dS K from the shared dS^T tile: into its own
+    // columns for d = 64; for d = 128 into the dP^T columns, after dK has read
+    // them (the tensor core runs this thread's instructions in issue order).
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
@@ -422,11 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tDK, sdesc_add(dS_k, off), sdesc_add(dQ_mn, kk * 2048), kIdV,
+          for (int kk = 0; kk < 8; ++kk)  // dS^T packed like P^T, in the dP^T columns
+            mma_ts(tDK, tDP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_add(dQ_mn, kk * 2048), kIdV,
                    kk > 0 ? 1u : acc0);
-          }
           tc_commit(bar(kBarQEmpty + s));
         }
         __syncwarp();
@@ -555,12 +555,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(kBarPReady));
         }
         if (!(ok = mbar_wait_warp(bar(kBarDPFull), g & 1, ctx, 0x232))) break;
-        if (g > 0 && !(ok = mbar_wait_warp(bar(kBarDSFree), (g - 1) & 1, ctx, 0x233))) break;
+        // dQ reads dS from the shared-memory tile: the previous one must be done
+        if (FUSED_DQ && g > 0 &&
+            !(ok = mbar_wait_warp(bar(kBarDSFree), (g - 1) & 1, ctx, 0x233)))
+          break;
         tc_fence_after();
         {
           const float4* Dv4 = reinterpret_cast<const float4*>(Dv);
-          // two 32-column chunks of dP^T; row r of the dS^T tile, 128-byte
-          // swizzle: 16-byte chunk c of the row lands at c ^ (r % 8)
+          // two 32-column chunks of dP^T.  dS^T goes back into the dP^T columns
+          // this warp has read, packed two queries per column as P^T is (the A
+          // operand of dK += dS^T Q), and for dQ into row r of the shared dS^T
+          // tile (128-byte swizzle: 16-byte chunk c lands at c ^ (r % 8)).
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             uint32_t u[32];
@@ -579,12 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           pack_bf16x2(__uint_as_float(u[4 * c4 + 2]) - dd.z,
                                                       __uint_as_float(u[4 * c4 + 3]) - dd.w));
             }
+            tmem_st16(tDP + 16 * ch, ds);
+            if constexpr (FUSED_DQ) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              st_shared_v4(sDSrow + (((4 * ch + c) ^ (r & 7)) << 4), ds[4 * c], ds[4 * c + 1],
-                           ds[4 * c + 2], ds[4 * c + 3]);
+              for (int c = 0; c < 4; ++c)
+                st_shared_v4(sDSrow + (((4 * ch + c) ^ (r & 7)) << 4), ds[4 * c], ds[4 * c + 1],
+                             ds[4 * c + 2], ds[4 * c + 3]);
+            }
           }
-          fence_proxy_async_smem();
+          tmem_wait_st();
+          if constexpr (FUSED_DQ) fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(bar(kBarDSReady));
         }
