@@ -10,9 +10,10 @@
 //    P^T = 2^(S^T s log2e - L log2e)    softmax warps, written back as bf16
 //    dP^T = V dO^T            (tensor memory)
 //    dV  += P^T dO            (A operand read from tensor memory)
-//    dS^T = P^T o (dP^T - D)  softmax warps, bf16 back into the dP^T
-//                             columns (and, for dQ, into shared memory)
-//    dK  += dS^T Q            (A operand read from tensor memory)
+//    dS^T = P^T o (dP^T - D)  softmax warps, bf16 into shared memory (for
+//                             dQ) or back into the dP^T columns
+//    dK  += dS^T Q            (A operand from shared memory, or from tensor
+//                              memory where dQ does not take the dP^T columns)
 //    dQ_i = dS K              (FUSED_DQ only: tensor memory, then staged
 //                              through shared memory and added into the fp32
 //                              accumulator by TMA reduce-add)
@@ -128,6 +129,12 @@ struct Layout {
   // dP columns once the softmax warps have read them.
   static constexpr bool kSeparateDq = HD == 64;
   static constexpr uint32_t kColDQ = kSeparateDq ? 2 * HD + 256 : kColDP;
+  // Where dQ shares the dP^T columns, dQ_i is issued before dK, so that its
+  // drain overlaps dK's contraction instead of holding back the next dP; dK
+  // then reads dS^T from shared memory (dQ has overwritten the columns).
+  // Elsewhere dK reads dS^T from the dP^T columns, packed there by the
+  // softmax warps, and no shared dS^T is needed without dQ.
+  static constexpr bool kDqFirst = FUSED_DQ && !kSeparateDq;
 };
 
 // Descriptor conventions (128-byte swizzle, tiles of 128 rows in 64-column
@@ -331,11 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dK_k = make_sdesc_sw128(sbase + Ly::kK, 16, 1024);        // K, K-major
     const uint64_t dK_mn = make_sdesc_sw128(sbase + Ly::kK, 16384, 1024);    // K, MN-major
     const uint64_t dV_k = make_sdesc_sw128(sbase + Ly::kV, 16, 1024);
+    const uint64_t dS_k = make_sdesc_sw128(sbase + Ly::kDS, 16, 1024);       // dS^T, K-major
     const uint64_t dS_mn = make_sdesc_sw128(sbase + Ly::kDS, 16384, 1024);   // dS, MN-major
     const uint32_t tS = tbase + Ly::kColS, tDP = tbase + Ly::kColDP;
     const uint32_t tDV = tbase + Ly::kColDV, tDK = tbase + Ly::kColDK;
     const uint32_t tDQ = tbase + Ly::kColDQ;
-    // Issue order per query tile:  dP, dV, S(next), dK, dQ.  S(next) goes right
+    // Issue order per query tile:  dP, dV, S(next), dQ, dK (d = 128 with dQ;
+    // else dK, dQ).  S(next) goes right
     // behind dV (which has consumed P from the S columns; the softmax warps
     // keep P in registers), so the softmax warps compute the next tile's P
     // while the tensor core runs dK and dQ.  The first S of an item waits for
@@ -349,10 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(bar(kBarSFull));
     };
-    // dK += dS^T Q with dS^T read from the dP^T columns (packed there by the
-    // softmax warps), then dQ_i = dS K from the shared dS^T tile: into its own
-    // columns for d = 64; for d = 128 into the dP^T columns, after dK has read
-    // them (the tensor core runs this thread's instructions in issue order).
+    // d = 128 with dQ: dQ_i = dS K into the dP^T columns (the softmax warps
+    // have read them), then dK += dS^T Q, both from the shared dS^T tile.
+    // Otherwise dK += dS^T Q with dS^T read from the dP^T columns (packed there
+    // by the softmax warps), then (d = 64) dQ_i = dS K into its own columns.
     bool ok = true;
     int g = 0;
     for (int k = 0, item = snake_item(0, b, G, n_items); ok && item >= 0; ++k) {
@@ -422,15 +431,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = mbar_wait_warp(bar(kBarDSReady), g & 1, ctx, 0x225))) break;
         tc_fence_after();
-        if (elect_one()) {
+        if constexpr (Ly::kDqFirst) {
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dS^T packed like P^T, in the dP^T columns
-            mma_ts(tDK, tDP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_add(dQ_mn, kk * 2048), kIdV,
-                   kk > 0 ? 1u : acc0);
-          tc_commit(bar(kBarQEmpty + s));
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tDQ, sdesc_add(dS_mn, kk * 2048), sdesc_add(dK_mn, kk * 2048), kIdQ,
+                     kk > 0 ? 1u : 0u);
+            tc_commit(bar(kBarDQFull));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              mma_ss(tDK, sdesc_add(dS_k, off), sdesc_add(dQ_mn, kk * 2048), kIdV,
+                     kk > 0 ? 1u : acc0);
+            }
+            tc_commit(bar(kBarQEmpty + s));
+          }
+          __syncwarp();
+        } else {
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // dS^T packed like P^T, in the dP^T columns
+              mma_ts(tDK, tDP + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_add(dQ_mn, kk * 2048),
+                     kIdV, kk > 0 ? 1u : acc0);
+            tc_commit(bar(kBarQEmpty + s));
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        if constexpr (FUSED_DQ) {
+        if constexpr (FUSED_DQ && !Ly::kDqFirst) {
           // With its own columns, dQ waits only for the previous dQ's drain.
           if (Ly::kSeparateDq && g > 0 &&
               !(ok = mbar_wait_warp(bar(kBarDQFree), (g - 1) & 1, ctx, 0x223)))
@@ -562,10 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         {
           const float4* Dv4 = reinterpret_cast<const float4*>(Dv);
-          // two 32-column chunks of dP^T.  dS^T goes back into the dP^T columns
-          // this warp has read, packed two queries per column as P^T is (the A
-          // operand of dK += dS^T Q), and for dQ into row r of the shared dS^T
-          // tile (128-byte swizzle: 16-byte chunk c lands at c ^ (r % 8)).
+          // two 32-column chunks of dP^T.  Where dK reads it from tensor memory,
+          // dS^T goes back into the dP^T columns this warp has read, packed two
+          // queries per column as P^T is; with dQ, into row r of the shared
+          // dS^T tile (128-byte swizzle: 16-byte chunk c lands at c ^ (r % 8)).
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             uint32_t u[32];
@@ -584,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           pack_bf16x2(__uint_as_float(u[4 * c4 + 2]) - dd.z,
                                                       __uint_as_float(u[4 * c4 + 3]) - dd.w));
             }
-            tmem_st16(tDP + 16 * ch, ds);
+            if constexpr (!Ly::kDqFirst) tmem_st16(tDP + 16 * ch, ds);
             if constexpr (FUSED_DQ) {
 #pragma unroll
               for (int c = 0; c < 4; ++c)
