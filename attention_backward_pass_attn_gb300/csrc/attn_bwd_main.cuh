@@ -73,7 +73,13 @@ constexpr int kBarDSFree = 18;
 constexpr int kBarDQFull = 19;
 constexpr int kBarDQFree = 20;
 constexpr int kBarDrain = 21;
-constexpr int kNumBars = 22;
+// The item epilogue stages dV and dK through the shared dS^T tile (two turns
+// for d = 128, one for d = 64): written by the softmax warps of a turn, then
+// stored by TMA, after which the tile is free again.  One pair per turn, so
+// that each barrier completes one phase per item.
+constexpr int kBarEpiFull = 22;   // + turn
+constexpr int kBarEpiFree = 24;   // + turn
+constexpr int kNumBars = 26;
 constexpr int kDrainBarrierId = 1;  // named barrier of the 128 dQ-drain threads
 
 // Work items are (head, key/value tile) pairs.  Heads are taken in groups
@@ -135,6 +141,9 @@ struct Layout {
   // Elsewhere dK reads dS^T from the dP^T columns, packed there by the
   // softmax warps, and no shared dS^T is needed without dQ.
   static constexpr bool kDqFirst = FUSED_DQ && !kSeparateDq;
+  // Turns of the item epilogue through the 32 KB dS^T tile: dV then dK for
+  // d = 128 (32 KB each), both at once for d = 64.
+  static constexpr int kEpiTurns = HD == 128 ? 2 : 1;
 };
 
 // Descriptor conventions (128-byte swizzle, tiles of 128 rows in 64-column
@@ -148,9 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO,
-                         const __grid_constant__ CUtensorMap tmAcc, const float* __restrict__ L2ws,
-                         const float* __restrict__ Dws,
-                         __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int BH,
+                         const __grid_constant__ CUtensorMap tmAcc,
+                         const __grid_constant__ CUtensorMap tmDK,
+                         const __grid_constant__ CUtensorMap tmDV, const float* __restrict__ L2ws,
+                         const float* __restrict__ Dws, int BH,
                          int N, int head_group, int window_arg, const int* __restrict__ doc,
                          int H, const int2* __restrict__ items, const int* __restrict__ qend,
                          const int* __restrict__ order, float scale, float scale_log2,
@@ -213,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t count =
           (i == kBarPReady || i == kBarDSReady || i == kBarAccEmpty) ? 256
           : (i == kBarDQFree)                                          ? 128
+          : (i == kBarEpiFull || i == kBarEpiFull + 1)                 ? 256 / Ly::kEpiTurns
                                                                        : 1;
       mbar_init(bar(i), count);
     }
@@ -582,9 +593,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(kBarPReady));
         }
         if (!(ok = mbar_wait_warp(bar(kBarDPFull), g & 1, ctx, 0x232))) break;
-        // dQ reads dS from the shared-memory tile: the previous one must be done
+        // dQ reads dS from the shared-memory tile: the previous one must be done,
+        // and at an item's first tile so must the previous item's epilogue
         if (FUSED_DQ && g > 0 &&
             !(ok = mbar_wait_warp(bar(kBarDSFree), (g - 1) & 1, ctx, 0x233)))
+          break;
+        if (FUSED_DQ && it == 0 && k > 0 &&
+            !(ok = mbar_wait_warp(bar(kBarEpiFree + Ly::kEpiTurns - 1), (k - 1) & 1, ctx,
+                                  0x234)))
           break;
         tc_fence_after();
         {
@@ -626,35 +642,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // Epilogue of the item: half 0 writes dV, half 1 writes dK (times the
-      // softmax scale), then the accumulators are released to the next item.
+      // Epilogue of the item: dV (half 0) and dK (half 1, times the softmax
+      // scale) from tensor memory, rounded to bf16 into the shared dS^T tile
+      // (its two 16 KB blocks are the 64-column boxes of the output tile map,
+      // with the same 128-byte swizzle) and written by TMA tile stores, which
+      // leave out the rows past N.  One elected warp per turn issues them;
+      // their shared-memory reads complete before the tile is used again.
       if (!(ok = mbar_wait_warp(bar(kBarAccFull), k & 1, ctx, 0x238 + h))) break;
       tc_fence_after();
-      const int kv = jt * 128 + r;
       const uint32_t tAcc = tbase + lane_off + (h == 0 ? Ly::kColDV : Ly::kColDK);
       const float mult = h == 0 ? 1.f : scale;
-      __nv_bfloat16* orow = (h == 0 ? dV : dK) + (size_t(bh) * N + kv) * HD;
+      for (int turn = 0; ok && turn < Ly::kEpiTurns; ++turn) {
+        if (Ly::kEpiTurns == 1 || h == turn) {
+          // The tile's previous contents: this item's dS^T (the contractions
+          // have completed: AccFull), then the previous turn's store -- of this
+          // item for turn 1, of the previous item for turn 0.
+          const int prev_turn = turn > 0 ? turn - 1 : Ly::kEpiTurns - 1;
+          const int prev_item = turn > 0 ? k : k - 1;
+          if (prev_item >= 0 &&
+              !(ok = mbar_wait_warp(bar(kBarEpiFree + prev_turn), prev_item & 1, ctx, 0x23A)))
+            break;
+          const uint32_t row = sbase + Ly::kDS + (HD == 64 ? h * 16384 : 0) + r * 128;
 #pragma unroll
-      for (int c4 = 0; c4 < HD / 32; ++c4) {
-        uint32_t o[32];
-        tmem_ld32(tAcc + 32 * c4, o);
-        tmem_wait_ld();
-        if (kv < N) {
+          for (int c4 = 0; c4 < HD / 32; ++c4) {
+            uint32_t o[32];
+            tmem_ld32(tAcc + 32 * c4, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint32_t w4[4];
+            for (int c8 = 0; c8 < 4; ++c8) {  // 16-byte chunk j of 64-column block c4 / 2
+              const int j = 4 * (c4 & 1) + c8;
+              uint32_t w4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w4[e] = pack_bf16x2(__uint_as_float(o[8 * c8 + 2 * e]) * mult,
-                                  __uint_as_float(o[8 * c8 + 2 * e + 1]) * mult);
-            st_global_v4(orow + 32 * c4 + 8 * c8, w4[0], w4[1], w4[2], w4[3]);
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16x2(__uint_as_float(o[8 * c8 + 2 * e]) * mult,
+                                    __uint_as_float(o[8 * c8 + 2 * e + 1]) * mult);
+              st_shared_v4(row + (c4 >> 1) * 16384 + ((j ^ (r & 7)) << 4), w4[0], w4[1], w4[2],
+                           w4[3]);
+            }
           }
+          tc_fence_before();
+          mbar_arrive(bar(kBarAccEmpty));  // this thread's accumulator columns are read
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kBarEpiFull + turn));
+        }
+        if (warp == 4 + 4 * (Ly::kEpiTurns == 2 ? turn : 0)) {  // the turn's issuing warp
+          if (!(ok = mbar_wait_warp(bar(kBarEpiFull + turn), k & 1, ctx, 0x23B))) break;
+          if (elect_one()) {
+            if constexpr (HD == 128) {
+              const CUtensorMap* map = turn == 0 ? &tmDV : &tmDK;
+              tma_store_3d(map, sbase + Ly::kDS, 0, jt * 128, bh);
+              tma_store_3d(map, sbase + Ly::kDS + 16384, 64, jt * 128, bh);
+            } else {
+              tma_store_3d(&tmDV, sbase + Ly::kDS, 0, jt * 128, bh);
+              tma_store_3d(&tmDK, sbase + Ly::kDS + 16384, 0, jt * 128, bh);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+            mbar_arrive(bar(kBarEpiFree + turn));
+          }
+          __syncwarp();
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(kBarAccEmpty));
+      if (!ok) break;
       item = snake_item(k + 1, b, G, n_items);
     }
+    bulk_wait_group_all();  // the epilogue's stores complete before the CTA retires
   } else if (FUSED_DQ) {
     // ------------------------------------------------------------ dQ drain
     // Tensor memory -> registers -> swizzled fp32 staging tile -> TMA
@@ -794,12 +846,14 @@ static cudaError_t launch_main_t(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   cudaError_t e =
       set_smem_limit_once<attn_bwd_main_kernel<HD, CAUSAL, MASK, FUSED_DQ>>(Ly::kBytes);
   if (e != cudaSuccess) return e;
+  // dK and dV are written by TMA tile stores: [BH][N][d] bf16, like Q.
+  CUtensorMap tmDK, tmDV;
+  if (make_tile_map(&tmDK, dK, s) || make_tile_map(&tmDV, dV, s)) return cudaErrorInvalidValue;
   // Persistent grid: at most one CTA per SM, each walking its work items.
   const long long n_items = (long long)s.n_tiles * s.BH;
   const dim3 grid(unsigned(n_items < num_sms() ? n_items : num_sms()));
   return launch_kernel(kern, grid, dim3(kThreads), Ly::kBytes, stream, tmQ, tmK, tmV, tmdO, tmAcc,
-                       ws.L2, ws.D, reinterpret_cast<__nv_bfloat16*>(dK),
-                       reinterpret_cast<__nv_bfloat16*>(dV), s.BH, s.N,
+                       tmDK, tmDV, ws.L2, ws.D, s.BH, s.N,
                        head_group(s, FUSED_DQ ? 8 : 4), s.window, s.doc, s.H,
                        static_cast<const int2*>(ws.items), static_cast<const int*>(ws.qend),
                        static_cast<const int*>(ws.order), scale, scale * 1.4426950408889634f,

@@ -191,6 +191,18 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       : "memory");
 }
 
+// Tiled 3-D store of a box from shared memory to global memory (coordinates
+// innermost first, >= 0; the parts of the box outside the tensor are not
+// written).  Completes as a bulk group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+          "l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // Bulk-group bookkeeping of the issuing thread.
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
