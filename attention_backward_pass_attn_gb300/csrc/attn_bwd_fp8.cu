@@ -300,16 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(bar(kBarDSReady), g & 1, ctx, 0x525))) break;
         tc_fence_after();
         if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
-            mma_ss_f8(tDK, sdesc_add(dS_k, kk * 32), sdesc_add(dQ_mn, kk * 4096), kIdV,
-                      kk > 0 ? 1u : acc0);
-          tc_commit(bar(kBarQEmpty + s));
+          // dQ first: its drain (which frees the dP^T columns for the next
+          // tile) then overlaps dK's contraction
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // dQ = dS K
             mma_ss_f8(tDQ, sdesc_add(dS_mn, kk * 4096), sdesc_add(dK_mn, kk * 4096), kIdQ,
                       kk > 0 ? 1u : 0u);
           tc_commit(bar(kBarDQFull));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
+            mma_ss_f8(tDK, sdesc_add(dS_k, kk * 32), sdesc_add(dQ_mn, kk * 4096), kIdV,
+                      kk > 0 ? 1u : acc0);
+          tc_commit(bar(kBarQEmpty + s));
           tc_commit(bar(kBarDSFree));
           if (last) {
             tc_commit(bar(kBarKEmpty));
