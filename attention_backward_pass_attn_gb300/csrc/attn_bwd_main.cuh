@@ -41,6 +41,7 @@
 // one-CTA sort (attn_bwd_order_kernel) orders the items by size.
 #pragma once
 
+#include "f32x2.cuh"
 #include "kernels.h"
 #include "mask.cuh"
 #include "ptx.cuh"
@@ -555,10 +556,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const float4 l = L2v4[c4];  // one broadcast load for four query columns
-            float p0 = ex2(fmaf(__uint_as_float(u[4 * c4]), scale_log2, -l.x));
-            float p1 = ex2(fmaf(__uint_as_float(u[4 * c4 + 1]), scale_log2, -l.y));
-            float p2 = ex2(fmaf(__uint_as_float(u[4 * c4 + 2]), scale_log2, -l.z));
-            float p3 = ex2(fmaf(__uint_as_float(u[4 * c4 + 3]), scale_log2, -l.w));
+            // y = L - s scale log2e for two columns per instruction; P = 2^-y
+            float y0, y1, y2, y3;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(u[4 * c4]), __uint_as_float(u[4 * c4 + 1])),
+                                  f32x2(-scale_log2, -scale_log2), f32x2(l.x, l.y)),
+                        y0, y1);
+            f32x2_split(
+                fma_f32x2(f32x2(__uint_as_float(u[4 * c4 + 2]), __uint_as_float(u[4 * c4 + 3])),
+                          f32x2(-scale_log2, -scale_log2), f32x2(l.z, l.w)),
+                y2, y3);
+            float p0 = ex2(-y0), p1 = ex2(-y1), p2 = ex2(-y2), p3 = ex2(-y3);
             if (diag) {  // key row r is visible to query columns >= r only
               const int q0 = 64 * h + 4 * c4;
               if (q0 < r) p0 = 0.f;
@@ -620,12 +627,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
               const float4 dd = Dv4[8 * ch + c4];  // one broadcast load for four columns
-              ds[2 * c4] = mul_bf16x2(pk[16 * ch + 2 * c4],
-                                      pack_bf16x2(__uint_as_float(u[4 * c4]) - dd.x,
-                                                  __uint_as_float(u[4 * c4 + 1]) - dd.y));
-              ds[2 * c4 + 1] = mul_bf16x2(pk[16 * ch + 2 * c4 + 1],
-                                          pack_bf16x2(__uint_as_float(u[4 * c4 + 2]) - dd.z,
-                                                      __uint_as_float(u[4 * c4 + 3]) - dd.w));
+              // dP - D for two columns per instruction (a product by -1 is exact)
+              float e0, e1, e2, e3;
+              f32x2_split(fma_f32x2(f32x2(dd.x, dd.y), f32x2(-1.f, -1.f),
+                                    f32x2(__uint_as_float(u[4 * c4]), __uint_as_float(u[4 * c4 + 1]))),
+                          e0, e1);
+              f32x2_split(
+                  fma_f32x2(f32x2(dd.z, dd.w), f32x2(-1.f, -1.f),
+                            f32x2(__uint_as_float(u[4 * c4 + 2]), __uint_as_float(u[4 * c4 + 3]))),
+                  e2, e3);
+              ds[2 * c4] = mul_bf16x2(pk[16 * ch + 2 * c4], pack_bf16x2(e0, e1));
+              ds[2 * c4 + 1] = mul_bf16x2(pk[16 * ch + 2 * c4 + 1], pack_bf16x2(e2, e3));
             }
             if constexpr (!Ly::kDqFirst) tmem_st16(tDP + 16 * ch, ds);
             if constexpr (FUSED_DQ) {
