@@ -17,7 +17,8 @@
 //    dQ_i = dS K              (FUSED_DQ only: tensor memory, then staged
 //                              through shared memory and added into the fp32
 //                              accumulator by TMA reduce-add)
-// dK and dV stay in tensor memory for the whole loop and are written once.
+// dK and dV stay in tensor memory for the whole loop and are written once, by
+// TMA tile stores from the dS^T tile (the item's epilogue).
 //
 // Warp roles (14 warps): 0-3 drain dQ from tensor memory into the
 // accumulator (idle without FUSED_DQ); 4-7 and 8-11 each own 64 of the 128
@@ -29,8 +30,9 @@
 // (dQ: its own columns for d = 64, the dP^T columns for d = 128).  Shared
 // memory: K, V, two stages of Q (with its per-row L and D vectors), dO (two
 // stages, except for d = 128 with FUSED_DQ, where the dQ staging buffers take
-// the room of the second), the dS^T tile and, with FUSED_DQ, two 16 KB fp32
-// staging buffers for the dQ reduction.
+// the room of the second), the dS^T tile (which also stages dV and dK at the
+// end of an item) and, with FUSED_DQ, two 16 KB fp32 staging buffers for the
+// dQ reduction.
 //
 // Work items are ordered heaviest first over all heads under the causal
 // mask, and in L2-sized groups of heads without it.  Mask variants (a causal

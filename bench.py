@@ -102,11 +102,12 @@ def _strip_comments(src: str) -> str:
 # The CUDA sources each profiled kernel is built from (its own code, the
 # PTX wrappers and mask helpers it includes, and its launcher).
 KERNEL_SOURCES = {
-    "attn_bwd_main_kernel": ["attn_bwd_main.cuh", "attn_bwd.cu", "ptx.cuh", "mask.cuh"],
+    "attn_bwd_main_kernel": ["attn_bwd_main.cuh", "attn_bwd.cu", "ptx.cuh", "mask.cuh",
+                             "f32x2.cuh", "kernels.h"],
     "attn_bwd_preprocess_kernel": ["attn_bwd.cu", "attn_bwd_main.cuh", "ptx.cuh", "mask.cuh"],
     "attn_bwd_dq_convert_kernel": ["attn_bwd.cu", "attn_bwd_main.cuh", "ptx.cuh", "mask.cuh"],
-    "attn_fwd_kernel": ["attn_fwd.cu", "ptx.cuh", "mask.cuh"],
-    "attn_fwd_fp8_kernel": ["attn_fwd_fp8.cu", "ptx.cuh"],
+    "attn_fwd_kernel": ["attn_fwd.cu", "ptx.cuh", "mask.cuh", "f32x2.cuh", "kernels.h"],
+    "attn_fwd_fp8_kernel": ["attn_fwd_fp8.cu", "ptx.cuh", "f32x2.cuh", "kernels.h"],
     "attn_bwd_fp8_kernel": ["attn_bwd_fp8.cu", "ptx.cuh"],
     "ssd_chunk_bwd_kernel": ["ssd.cu", "ptx.cuh"],
 }
