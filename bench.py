@@ -452,12 +452,15 @@ def time_fp8_backward(w, steps: int, warmup: int, flush):
     return [a.elapsed_time(b) for a, b in rec]
 
 
-def e2e_workload(w, steps: int, warmup: int):
-    """The step through the public API with pinned host buffers, pipelined as a
-    training loop would run it: each step copies its inputs host -> device,
-    runs attn_fwd and attn_bwd, and copies its gradients device -> host; the
-    copies run on their own streams, so step i+1's upload and step i-1's
-    download overlap step i's compute (two sets of device buffers).
+def e2e_workload(w, steps: int, warmup: int, with_forward: bool = False):
+    """The backward through the public API with pinned host buffers, pipelined
+    as a training loop would run it: each step copies the backward's inputs
+    (Q, K, V, O, dO and L) host -> device, runs attn_bwd, and copies dQ, dK,
+    dV device -> host; the copies run on their own streams, so step i+1's
+    upload and step i-1's download overlap step i's compute (two sets of device
+    buffers).  O and L come from one attn_fwd before the loop.  With
+    `with_forward`, each step instead uploads Q, K, V, dO and runs attn_fwd
+    then attn_bwd (a whole attention training step).
     Returns (ms per step over the timed steps, h2d bytes, d2h bytes, device
     bytes of both buffer sets)."""
     import torch
@@ -466,15 +469,24 @@ def e2e_workload(w, steps: int, warmup: int):
     from attention_backward_pass_attn_gb300.inputs import make_inputs
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    host_in = [t.pin_memory() for t in make_inputs(w)]
+    q, k, v, do = make_inputs(w)
+    if with_forward:
+        host_in = [t.pin_memory() for t in (q, k, v, do)]
+    else:
+        qd, kd, vd = (t.to(dev) for t in (q, k, v))
+        o, lse = ab.attn_fwd(qd, kd, vd, w.causal, w.scale)
+        torch.cuda.synchronize()
+        host_in = [t.pin_memory() for t in (q, k, v, o.cpu(), do, lse.cpu())]
+        del qd, kd, vd, o, lse
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in host_in[:3]]
     sets = []
     for _ in range(2):
         dev_in = [torch.empty_like(t, device=dev) for t in host_in]
         sets.append({
             "in": dev_in,
-            "o": torch.empty_like(dev_in[0]),
-            "lse": torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev),
+            "o": torch.empty_like(dev_in[0]) if with_forward else None,
+            "lse": (torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+                    if with_forward else None),
             "grads": [torch.empty_like(dev_in[0]) for _ in range(3)],
             "ws": ab.alloc_workspace(w.B, w.H, w.N, w.d, dev),
             "in_ready": torch.cuda.Event(), "done": torch.cuda.Event(),
@@ -499,9 +511,13 @@ def e2e_workload(w, steps: int, warmup: int):
             s_comp.wait_event(b["in_ready"])
             if i >= 2:
                 s_comp.wait_event(b["out_free"])
-            q, k, v, do = b["in"]
-            ab.attn_fwd(q, k, v, w.causal, w.scale, out=b["o"], lse=b["lse"], stream=s_comp)
-            ab.attn_bwd(q, k, v, b["o"], do, b["lse"], w.causal, w.scale, dq=b["grads"][0],
+            if with_forward:
+                q_, k_, v_, do_ = b["in"]
+                o_, lse_ = b["o"], b["lse"]
+                ab.attn_fwd(q_, k_, v_, w.causal, w.scale, out=o_, lse=lse_, stream=s_comp)
+            else:
+                q_, k_, v_, o_, do_, lse_ = b["in"]
+            ab.attn_bwd(q_, k_, v_, o_, do_, lse_, w.causal, w.scale, dq=b["grads"][0],
                         dk=b["grads"][1], dv=b["grads"][2], workspace=b["ws"], stream=s_comp)
             b["in_free"].record(s_comp)
             b["done"].record(s_comp)
@@ -517,7 +533,7 @@ def e2e_workload(w, steps: int, warmup: int):
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     resident = 0
     for b in sets:
-        for t in b["in"] + b["grads"] + [b["o"], b["lse"], b["ws"]]:
+        for t in b["in"] + b["grads"] + [b["ws"]] + ([b["o"], b["lse"]] if with_forward else []):
             resident += t.numel() * t.element_size()
     return ms, h2d, d2h, resident
 
@@ -624,6 +640,10 @@ def run_ours(args):
     e2e_ms, h2d, d2h, e2e_resident = e2e_workload(w, e2e_steps, 3)
     e2e_max, e2e_flops = aggregate(e2e_ms * e2e_steps, w.bwd_flops() * e2e_steps)
     e2e_value = e2e_flops / (e2e_max * 1e-3) / 1e12
+    # the same pipeline around a whole attention training step (attn_fwd then
+    # attn_bwd), reported beside it
+    ts_ms, ts_h2d, ts_d2h, _ = e2e_workload(w, e2e_steps, 3, with_forward=True)
+    ts_max, ts_flops = aggregate(ts_ms * e2e_steps, w.bwd_flops() * e2e_steps)
 
     extra = None
     if not args.no_extra:
@@ -758,11 +778,19 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5), "steps": e2e_steps,
-                "what": "pinned host inputs -> device, attn_fwd, attn_bwd, gradients -> host "
-                        "every step; copies on their own streams overlap neighbouring steps' "
-                        "compute (two device buffer sets); backward FLOPs / step time",
+                "what": "the backward through the public API: its inputs (Q, K, V, O, dO, L) "
+                        "pinned host -> device, attn_bwd, dQ/dK/dV -> host every step; copies "
+                        "on their own streams overlap neighbouring steps' compute (two device "
+                        "buffer sets); backward FLOPs / step time",
                 "l2": "not flushed: the two alternating device buffer sets hold %.0f MiB, "
-                      "more than the 129 MB L2" % (e2e_resident / 2**20)},
+                      "more than the 129 MB L2" % (e2e_resident / 2**20),
+                "training_step": {
+                    "value": round(ts_flops / (ts_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "ms_per_step": round(ts_ms, 5), "h2d_bytes_per_step": ts_h2d,
+                    "d2h_bytes_per_step": ts_d2h,
+                    "what": "the same pipeline around attn_fwd then attn_bwd (Q, K, V, dO "
+                            "uploaded); backward FLOPs / step time, the forward's time "
+                            "included"}},
         "roofline": {
             "kernel": "attn_bwd_main_kernel", "bound": "tensor",
             "achieved": round(achieved, 2), "peak": peak_used, "unit": "TFLOP/s",
