@@ -373,12 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // row may see (sliding window, document)
         const bool below = MASK != kMaskPlain && kv0 < lo_q;
         if ((CAUSAL && kv0 + 127 > q_tile0) || kv0 + 128 > N || below) {
+          // the row sees columns e_lo .. e_hi of this tile
+          const int e_hi = min(CAUSAL ? q - kv0 : 127, N - 1 - kv0);
+          const int e_lo = below ? lo_q - kv0 : 0;
 #pragma unroll
-          for (int e = 0; e < 128; ++e) {
-            const int kv = kv0 + e;
-            if ((CAUSAL && kv > q) || kv >= N || (below && kv < lo_q))
-              u[e] = __float_as_uint(-INFINITY);
-          }
+          for (int e = 0; e < 128; ++e)
+            if (e > e_hi || e < e_lo) u[e] = __float_as_uint(-INFINITY);
         }
         // row maximum: eight chains of three-input maxima (two scores each)
         float m8[8];
