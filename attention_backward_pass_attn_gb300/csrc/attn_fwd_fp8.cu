@@ -293,11 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         const int kv0 = j * 128;
         if ((CAUSAL && kv0 + 127 > q_tile0) || kv0 + 128 > N) {
+          const int e_hi = min(CAUSAL ? q - kv0 : 127, N - 1 - kv0);  // last visible column
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int kv = kv0 + c;
-            if ((CAUSAL && kv > q) || kv >= N) u[c] = __float_as_uint(-INFINITY);
-          }
+          for (int c = 0; c < 128; ++c)
+            if (c > e_hi) u[c] = __float_as_uint(-INFINITY);
         }
         // row maximum: eight chains of three-input maxima (two scores each)
         float m8[8];
