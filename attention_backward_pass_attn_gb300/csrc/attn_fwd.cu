@@ -25,7 +25,8 @@
 //  * While the softmax of tile A runs, the tensor core works on tile B, and
 //    the next S of one tile is computed while the other tile's P V runs.
 //  * Causal: a task stops at the last key tile its rows can see; tiles on the
-//    diagonal are masked element-wise.  Tasks are taken heaviest first.
+//    diagonal are masked element-wise, each row against the first and last
+//    column it may see.  Tasks are taken heaviest first.
 //    Without the mask they run head by head, so the CTAs working at one time
 //    share K and V in L2.
 //  * Mask variants (mask.cuh: a causal sliding window, documents of packed
