@@ -109,6 +109,7 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd.cu", "ptx.cuh", "mask.cuh", "f32x2.cuh", "kernels.h"],
     "attn_fwd_fp8_kernel": ["attn_fwd_fp8.cu", "ptx.cuh", "f32x2.cuh", "kernels.h"],
     "attn_bwd_fp8_kernel": ["attn_bwd_fp8.cu", "ptx.cuh"],
+    "attn_bwd_dq_kernel": ["attn_bwd_dq.cu", "ptx.cuh", "mask.cuh", "kernels.h"],
     "ssd_chunk_bwd_kernel": ["ssd.cu", "ptx.cuh"],
 }
 
