@@ -104,6 +104,9 @@ def _strip_comments(src: str) -> str:
 KERNEL_SOURCES = {
     "attn_bwd_main_kernel": ["attn_bwd_main.cuh", "attn_bwd.cu", "ptx.cuh", "mask.cuh",
                              "f32x2.cuh", "kernels.h"],
+    # the same template without dQ (the separate-dQ method's first pass)
+    "attn_bwd_main_kernel_dkdv": ["attn_bwd_main.cuh", "attn_bwd.cu", "ptx.cuh", "mask.cuh",
+                                  "f32x2.cuh", "kernels.h"],
     "attn_bwd_preprocess_kernel": ["attn_bwd.cu", "attn_bwd_main.cuh", "ptx.cuh", "mask.cuh"],
     "attn_bwd_dq_convert_kernel": ["attn_bwd.cu", "attn_bwd_main.cuh", "ptx.cuh", "mask.cuh"],
     "attn_fwd_kernel": ["attn_fwd.cu", "ptx.cuh", "mask.cuh", "f32x2.cuh", "kernels.h"],

@@ -102,6 +102,23 @@ def test_kernel_hash_covers_its_sources(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("k") != h0
 
 
+def test_committed_ncu_entries_match_their_sources():
+    """Every committed ncu entry names a kernel whose CUDA sources are known and
+    still hash to the value recorded with it: a kernel change needs a new
+    capture (or the entry's removal) before its counters are reported."""
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        table = json.load(f)
+    assert table
+    for key, ent in table.items():
+        kernel, _, workload = key.partition("@")
+        assert workload, key
+        assert kernel in bench.KERNEL_SOURCES, key
+        assert ent["source_hash"] == bench.kernel_source_hash(kernel), key
+        assert ent["dram_bytes_per_launch"] == ent["dram_read_bytes"] + ent["dram_write_bytes"], key
+        assert "--clock-control none" in ent["command"], key
+        assert bench.stored_ncu(kernel, workload) is ent or bench.stored_ncu(kernel, workload) == ent
+
+
 def test_reference_arm_runs_on_cpu():
     p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--workload", "b1h2n128d64", "--steps", "2", "--warmup", "1"],
