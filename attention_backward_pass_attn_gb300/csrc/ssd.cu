@@ -269,53 +269,64 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ------------------------------------------------------------------ step 2
-// One thread per (b, h, state element): the prefix scan of the states over
-// chunks (S becomes H_in, the state entering each chunk) and, for the
-// backward, the reverse scan of the state gradient (R becomes dH_out, the
-// gradient of the state leaving each chunk from the chunks after it).
+// The prefix scan of the states over chunks (S becomes H_in, the state
+// entering each chunk) and, for the backward, the reverse scan of the state
+// gradient (R becomes dH_out, the gradient of the state leaving each chunk
+// from the chunks after it).  Each thread carries four consecutive state
+// elements of one (b, h) with 16-byte accesses, so a block reads and writes
+// 4 KB runs of each chunk's state; every element's multiply-adds are those of
+// a one-element scan, in the same order.
+__device__ __forceinline__ float4 scan_step(float a, float4 carry, float4 v) {
+  return make_float4(fmaf(a, carry.x, v.x), fmaf(a, carry.y, v.y), fmaf(a, carry.z, v.z),
+                     fmaf(a, carry.w, v.w));
+}
+
 __global__ void __launch_bounds__(kThreads)
     ssd_state_scan_kernel(float* __restrict__ S, float* __restrict__ R,
                           const float* __restrict__ dec, int NP, Dims d, int bwd) {
-  const int e = blockIdx.x * kThreads + threadIdx.x;
+  const int e = 4 * (blockIdx.x * kThreads + threadIdx.x);  // NP is a multiple of 4 kThreads
   const int h = blockIdx.y, b = blockIdx.z;
   grid_dep_wait();
   grid_dep_launch();
   if (e >= NP) return;
   const size_t base = (size_t(b) * d.H + h) * d.nc;
+  auto at = [&](float* M, int c) { return reinterpret_cast<float4*>(M + (base + c) * NP + e); };
   // Sixteen chunks' values are loaded before any is used: the loads do not
   // depend on the carry, only the multiply-adds do.
   constexpr int U = 16;
-  float carry = 0.f;
+  float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c0 = 0; c0 < d.nc; c0 += U) {
-    float v[U], a[U];
+    float4 v[U];
+    float a[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 + u;
-      v[u] = c < d.nc ? S[(base + c) * NP + e] : 0.f;
+      v[u] = c < d.nc ? *at(S, c) : make_float4(0.f, 0.f, 0.f, 0.f);
       a[u] = c < d.nc ? dec[base + c] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 + u;
-      if (c < d.nc) S[(base + c) * NP + e] = carry;
-      carry = fmaf(a[u], carry, v[u]);
+      if (c < d.nc) *at(S, c) = carry;
+      carry = scan_step(a[u], carry, v[u]);
     }
   }
   if (!bwd) return;
-  carry = 0.f;
+  carry = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c0 = d.nc - 1; c0 >= 0; c0 -= U) {
-    float v[U], a[U];
+    float4 v[U];
+    float a[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 - u;
-      v[u] = c >= 0 ? R[(base + c) * NP + e] : 0.f;
+      v[u] = c >= 0 ? *at(R, c) : make_float4(0.f, 0.f, 0.f, 0.f);
       a[u] = c >= 0 ? dec[base + c] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 - u;
-      if (c >= 0) R[(base + c) * NP + e] = carry;
-      carry = fmaf(a[u], carry, v[u]);
+      if (c >= 0) *at(R, c) = carry;
+      carry = scan_step(a[u], carry, v[u]);
     }
   }
 }
@@ -831,7 +842,8 @@ static cudaError_t run(const SsdArgs& a, cudaStream_t st) {
                       x, a.dt, a.A, Bm, Cm, dy, a.ws_S, a.ws_R, a.ws_dec, d);
   if (e != cudaSuccess) return e;
   const int NP = N * P;
-  e = launch_kernel(ssd_state_scan_kernel, dim3(unsigned(NP / kThreads), a.H, a.Bt),
+  static_assert(N * P % (4 * kThreads) == 0, "the scan takes four state elements a thread");
+  e = launch_kernel(ssd_state_scan_kernel, dim3(unsigned(NP / (4 * kThreads)), a.H, a.Bt),
                     dim3(kThreads), 0, st, a.ws_S, a.ws_R, static_cast<const float*>(a.ws_dec),
                     NP, d, bwd ? 1 : 0);
   if (e != cudaSuccess) return e;
