@@ -99,46 +99,58 @@ __device__ __forceinline__ float get(const float4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
-// Loads the chunk's rows of a [Bt][T][X][W] bf16 tensor (index xi along X)
-// into shared memory as fp32 rows of stride `ld`, four values per thread and
-// step; rows past T are zero.
+// A chunk's rows of a [Bt][T][X][W] bf16 tensor (index xi along X), held in
+// registers between load() and store(), so that a kernel issues the loads of
+// all its tiles before it waits for any.  store() writes them to shared
+// memory as fp32 rows of stride `ld`, four values per thread and step; rows
+// past T are zero.
 template <int W>
-__device__ __forceinline__ void load_rows(float* dst, int ld, const uint16_t* src, const Dims& d,
-                                          int X, int b, int t0, int xi) {
-  constexpr int kIter = Lc * W / 4 / kThreads;  // 4-value groups per thread
+struct RowTile {
+  static constexpr int kIter = Lc * W / 4 / kThreads;  // 4-value groups per thread
   static_assert(kIter * kThreads * 4 == Lc * W, "tile not a whole number of passes");
   uint2 r[kIter];
+  __device__ __forceinline__ void load(const uint16_t* src, const Dims& d, int X, int b, int t0,
+                                       int xi) {
 #pragma unroll
-  for (int k = 0; k < kIter; ++k) {  // every load issued before any is used
-    const int idx = threadIdx.x + k * kThreads;
-    const int i = idx / (W / 4), w = (idx - i * (W / 4)) * 4;
-    const int t = t0 + i;
-    r[k] = t < d.T ? *reinterpret_cast<const uint2*>(src + ((size_t(b) * d.T + t) * X + xi) * W + w)
-                   : make_uint2(0u, 0u);
+    for (int k = 0; k < kIter; ++k) {
+      const int idx = threadIdx.x + k * kThreads;
+      const int i = idx / (W / 4), w = (idx - i * (W / 4)) * 4;
+      const int t = t0 + i;
+      r[k] = t < d.T
+                 ? *reinterpret_cast<const uint2*>(src + ((size_t(b) * d.T + t) * X + xi) * W + w)
+                 : make_uint2(0u, 0u);
+    }
   }
+  __device__ __forceinline__ void store(float* dst, int ld) const {
 #pragma unroll
-  for (int k = 0; k < kIter; ++k) {
-    const int idx = threadIdx.x + k * kThreads;
-    const int i = idx / (W / 4), w = (idx - i * (W / 4)) * 4;
-    *reinterpret_cast<float4*>(dst + i * ld + w) =
-        make_float4(__uint_as_float(r[k].x << 16), __uint_as_float(r[k].x & 0xFFFF0000u),
-                    __uint_as_float(r[k].y << 16), __uint_as_float(r[k].y & 0xFFFF0000u));
+    for (int k = 0; k < kIter; ++k) {
+      const int idx = threadIdx.x + k * kThreads;
+      const int i = idx / (W / 4), w = (idx - i * (W / 4)) * 4;
+      *reinterpret_cast<float4*>(dst + i * ld + w) =
+          make_float4(__uint_as_float(r[k].x << 16), __uint_as_float(r[k].x & 0xFFFF0000u),
+                      __uint_as_float(r[k].y << 16), __uint_as_float(r[k].y & 0xFFFF0000u));
+    }
   }
-}
+};
 
-// Loads a transposed state [P][N] fp32 of one chunk into shared memory.
+// A transposed state [P][N] fp32 of one chunk, held in registers between
+// load() and store() (rows of stride N + 4 in shared memory).
 template <int N, int P>
-__device__ __forceinline__ void load_state(float* dst, const float* __restrict__ src) {
-  constexpr int kIter = N * P / 4 / kThreads;
+struct StateTile {
+  static constexpr int kIter = N * P / 4 / kThreads;
   float4 v[kIter];
+  __device__ __forceinline__ void load(const float* __restrict__ src) {
 #pragma unroll
-  for (int k = 0; k < kIter; ++k) v[k] = ld4(src + (threadIdx.x + k * kThreads) * 4);
-#pragma unroll
-  for (int k = 0; k < kIter; ++k) {
-    const int e = (threadIdx.x + k * kThreads) * 4;
-    *reinterpret_cast<float4*>(dst + (e / N) * (N + 4) + e % N) = v[k];
+    for (int k = 0; k < kIter; ++k) v[k] = ld4(src + (threadIdx.x + k * kThreads) * 4);
   }
-}
+  __device__ __forceinline__ void store(float* dst) const {
+#pragma unroll
+    for (int k = 0; k < kIter; ++k) {
+      const int e = (threadIdx.x + k * kThreads) * 4;
+      *reinterpret_cast<float4*>(dst + (e / N) * (N + 4) + e % N) = v[k];
+    }
+  }
+};
 
 // dt of the chunk, cs = inclusive cumulative sum of dt A, e_in = exp(cs),
 // e_out = exp(cs_end - cs).  Steps past T have dt = 0 (no decay, no input).
@@ -217,12 +229,22 @@ __global__ void __launch_bounds__(kThreads)
   float* vec = sm + Ly::oVec;
   grid_dep_wait();
   grid_dep_launch();
-  chunk_decays(vec, dt, d, b, h, t0, A[h]);
-  load_rows<P>(sm + Ly::oX, Ly::XS, x, d, d.H, b, t0, h);
-  load_rows<N>(sm + Ly::oB, Ly::BS, Bm, d, d.G, b, t0, g);
+  // every tile's loads go out before the decays are formed and before any
+  // tile is stored
+  RowTile<P> inX, inDY;
+  RowTile<N> inB, inC;
+  inX.load(x, d, d.H, b, t0, h);
+  inB.load(Bm, d, d.G, b, t0, g);
   if (BWD) {
-    load_rows<P>(sm + Ly::oDY, Ly::XS, dy, d, d.H, b, t0, h);
-    load_rows<N>(sm + Ly::oC, Ly::BS, Cm, d, d.G, b, t0, g);
+    inDY.load(dy, d, d.H, b, t0, h);
+    inC.load(Cm, d, d.G, b, t0, g);
+  }
+  chunk_decays(vec, dt, d, b, h, t0, A[h]);
+  inX.store(sm + Ly::oX, Ly::XS);
+  inB.store(sm + Ly::oB, Ly::BS);
+  if (BWD) {
+    inDY.store(sm + Ly::oDY, Ly::XS);
+    inC.store(sm + Ly::oC, Ly::BS);
   }
   __syncthreads();
   const size_t chunk = (size_t(b) * d.H + h) * d.nc + c;
@@ -356,13 +378,24 @@ __global__ void __launch_bounds__(kThreads)
   const size_t chunk = (size_t(b) * d.H + h) * d.nc + c;
   grid_dep_wait();
   grid_dep_launch();
+  // every tile's loads go out before the decays are formed and before any
+  // tile is stored
+  RowTile<P> inX, inDY;
+  RowTile<N> inB, inC;
+  StateTile<N, P> inH, indH;
+  inX.load(x, d, d.H, b, t0, h);
+  inDY.load(dy, d, d.H, b, t0, h);
+  inB.load(Bm, d, d.G, b, t0, g);
+  inC.load(Cm, d, d.G, b, t0, g);
+  inH.load(Hin + chunk * N * P);
+  indH.load(dHout + chunk * N * P);
   chunk_decays(vec, dt, d, b, h, t0, Ah);
-  load_rows<P>(sm + Ly::oX, Ly::XS, x, d, d.H, b, t0, h);
-  load_rows<P>(sm + Ly::oDY, Ly::XS, dy, d, d.H, b, t0, h);
-  load_rows<N>(sm + Ly::oB, Ly::BS, Bm, d, d.G, b, t0, g);
-  load_rows<N>(sm + Ly::oC, Ly::BS, Cm, d, d.G, b, t0, g);
-  load_state<N, P>(sm + Ly::oH, Hin + chunk * N * P);
-  load_state<N, P>(sm + Ly::odH, dHout + chunk * N * P);
+  inX.store(sm + Ly::oX, Ly::XS);
+  inDY.store(sm + Ly::oDY, Ly::XS);
+  inB.store(sm + Ly::oB, Ly::BS);
+  inC.store(sm + Ly::oC, Ly::BS);
+  inH.store(sm + Ly::oH);
+  indH.store(sm + Ly::odH);
   __syncthreads();
   const float* Xs = sm + Ly::oX;
   const float* DYs = sm + Ly::oDY;
@@ -377,6 +410,13 @@ __global__ void __launch_bounds__(kThreads)
   const float* ein = vec + vEIN * Lc;
   const float* eout = vec + vEOUT * Lc;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  // Row block (of 4 rows) of this half-warp in the triangular steps B-D.  B
+  // and C run over rows i >= j, D over j <= i, so a low block costs more in
+  // B and C and less in D.  Warps w and w + 4 share an SM sub-partition:
+  // warp w takes blocks 2w, 2w + 1 and warp w + 4 blocks 14 - 2w, 15 - 2w,
+  // which gives every sub-partition the same share of the triangles.
+  const int warp_id = threadIdx.x >> 5;
+  const int rb = 2 * (warp_id < 4 ? warp_id : 11 - warp_id) + (ty & 1);
 
   // ---- A: C B^T and dy x^T, masked and decayed; the pair sums for ddt.
   // Thread tile: rows i = 4 ty + a, columns j = tx + 16 q.
@@ -420,9 +460,9 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // ---- B: dx_j = dt_j (sum_i M1[i][j] dy_i + e_out[j] dH^T B_j) + D dy_j.
-  // Thread tile: rows j = 4 ty + a, channels p = tx + 16 e.
+  // Thread tile: rows j = 4 rb + a, channels p = tx + 16 e.
   {
-    const int j0 = ty * 4;
+    const int j0 = rb * 4;
     float in[4][4] = {}, out[4][4] = {};
     for (int i = j0; i < Lc; ++i) {  // M1[i][j] = 0 for i < j
       const float4 mv = ld4(M1 + i * Ly::MS + j0);
@@ -464,9 +504,9 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---- C: dB_j = dt_j (sum_i M2[i][j] C_i + e_out[j] dH x_j),
   //         F_j / dt_j = B_j . (e_out[j] dH x_j)
-  // Thread tile: rows j = 4 ty + a, states n = 4 tx + 64 u + e.
+  // Thread tile: rows j = 4 rb + a, states n = 4 tx + 64 u + e.
   {
-    const int j0 = ty * 4, n0 = tx * 4;
+    const int j0 = rb * 4, n0 = tx * 4;
     float in[4][NU][4] = {}, out[4][NU][4] = {};
     for (int i = j0; i < Lc; ++i) {
       const float4 mv = ld4(M2 + i * Ly::MS + j0);
@@ -528,9 +568,9 @@ __global__ void __launch_bounds__(kThreads)
 
   // ---- D: dC_i = sum_j M2[i][j] dt_j B_j + e_in[i] H dy_i,
   //         E_i = C_i . (e_in[i] H dy_i)
-  // Thread tile: rows i = 4 ty + a, states n = 4 tx + 64 u + e.
+  // Thread tile: rows i = 4 rb + a, states n = 4 tx + 64 u + e.
   {
-    const int i0 = ty * 4, n0 = tx * 4;
+    const int i0 = rb * 4, n0 = tx * 4;
     float in[4][NU][4] = {}, out[4][NU][4] = {};
     for (int j = 0; j <= i0 + 3; j += 4) {  // M2[i][j] = 0 for j > i
       float4 mv[4];
@@ -750,11 +790,20 @@ __global__ void __launch_bounds__(kThreads)
   const size_t chunk = (size_t(b) * d.H + h) * d.nc + c;
   grid_dep_wait();
   grid_dep_launch();
+  // every tile's loads go out before the decays are formed and before any
+  // tile is stored
+  RowTile<P> inX;
+  RowTile<N> inB, inC;
+  StateTile<N, P> inH;
+  inX.load(x, d, d.H, b, t0, h);
+  inB.load(Bm, d, d.G, b, t0, g);
+  inC.load(Cm, d, d.G, b, t0, g);
+  inH.load(Hin + chunk * N * P);
   chunk_decays(vec, dt, d, b, h, t0, A[h]);
-  load_rows<P>(sm + Ly::oX, Ly::XS, x, d, d.H, b, t0, h);
-  load_rows<N>(sm + Ly::oB, Ly::BS, Bm, d, d.G, b, t0, g);
-  load_rows<N>(sm + Ly::oC, Ly::BS, Cm, d, d.G, b, t0, g);
-  load_state<N, P>(sm + Ly::oH, Hin + chunk * N * P);
+  inX.store(sm + Ly::oX, Ly::XS);
+  inB.store(sm + Ly::oB, Ly::BS);
+  inC.store(sm + Ly::oC, Ly::BS);
+  inH.store(sm + Ly::oH);
   __syncthreads();
   const float* Xs = sm + Ly::oX;
   const float* Bs = sm + Ly::oB;
@@ -778,12 +827,18 @@ __global__ void __launch_bounds__(kThreads)
       }
   }
   __syncthreads();
-  // rows i = 4 ty + a, channels p = tx + 16 e
+  // rows i = 4 rb + a, channels p = tx + 16 e.  The triangle is longest for
+  // the last row blocks: warp w takes blocks 2w, 2w + 1 and warp w + 4 (on the
+  // same SM sub-partition) blocks 14 - 2w, 15 - 2w, which evens the
+  // sub-partitions' shares.
+  const int warp_id = threadIdx.x >> 5;
+  const int rb = 2 * (warp_id < 4 ? warp_id : 11 - warp_id) + (ty & 1);
+  const int i1 = rb * 4;
   float in[4][4] = {}, out[4][4] = {};
-  for (int j = 0; j <= i0 + 3; j += 4) {  // M1[i][j] = 0 for j > i
+  for (int j = 0; j <= i1 + 3; j += 4) {  // M1[i][j] = 0 for j > i
     float4 mv[4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) mv[a] = ld4(M1 + (i0 + a) * Ly::MS + j);
+    for (int a = 0; a < 4; ++a) mv[a] = ld4(M1 + (i1 + a) * Ly::MS + j);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       float xv[4];
@@ -795,11 +850,11 @@ __global__ void __launch_bounds__(kThreads)
         for (int e = 0; e < 4; ++e) in[a][e] = fmaf(get(mv[a], kk), xv[e], in[a][e]);
     }
   }
-  rows_dot<N>(out, Cs, HT, Ly::BS, i0, tx);  // sum_n C_i[n] H^T[p][n], p = tx + 16 e
+  rows_dot<N>(out, Cs, HT, Ly::BS, i1, tx);  // sum_n C_i[n] H^T[p][n], p = tx + 16 e
   const float Dh = D[h];
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
-    const int i = i0 + a, t = t0 + i;
+    const int i = i1 + a, t = t0 + i;
     if (t >= d.T) continue;
     float* row = y + ((size_t(b) * d.T + t) * d.H + h) * P;
 #pragma unroll
