@@ -61,6 +61,15 @@ HEADLINE = "b4h16n8192d128"
 OTHER = ["b2h16n2048d64_causal", "b1h32n4096d128_causal", "b1h16n16384d128_causal"]
 METRIC = "attention backward TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 peak"
 FLUSH_BYTES = 512 << 20
+# The extra workloads' timing: 10 warm-ups, then the median of 50 steps (200
+# on the small d = 64 workloads, whose steps take tens of microseconds).
+EXTRA_WARMUP = 10
+EXTRA_REPS = 50
+SMALL_REPS = 200
+
+
+def extra_reps(w) -> int:
+    return SMALL_REPS if w.d == 64 else EXTRA_REPS
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -654,8 +663,8 @@ def run_ours(args):
         extra = {}
         for name in OTHER:
             ow = WORKLOADS[name]
-            r = time_workload(ow, 10, 3, flush, split=True)
-            rw = time_workload(ow, 10, 3, flush)
+            r = time_workload(ow, extra_reps(ow), EXTRA_WARMUP, flush, split=True)
+            rw = time_workload(ow, extra_reps(ow), EXTRA_WARMUP, flush)
             mm = statistics.median(r["main"])
             extra[name] = {
                 "bwd_main_tflops": round(ow.bwd_flops() / mm / 1e9, 1),
@@ -672,9 +681,10 @@ def run_ours(args):
         cmp = {}
         for name in [w.name] + OTHER:
             cw = w if name == w.name else WORKLOADS[name]
-            red = time_workload(cw, 10, 3, flush, dq_method=ATTN_DQ_REDUCE)
-            sep = time_workload(cw, 10, 3, flush, dq_method=ATTN_DQ_SEPARATE)
-            sep_split = time_workload(cw, 10, 3, flush, split=True, dq_method=ATTN_DQ_SEPARATE)
+            n, wu = extra_reps(cw), EXTRA_WARMUP
+            red = time_workload(cw, n, wu, flush, dq_method=ATTN_DQ_REDUCE)
+            sep = time_workload(cw, n, wu, flush, dq_method=ATTN_DQ_SEPARATE)
+            sep_split = time_workload(cw, n, wu, flush, split=True, dq_method=ATTN_DQ_SEPARATE)
             r_ms, s_ms = statistics.median(red["bwd"]), statistics.median(sep["bwd"])
             cmp[name] = {
                 "reduce_bwd_ms": round(r_ms, 4), "separate_bwd_ms": round(s_ms, 4),
@@ -690,9 +700,9 @@ def run_ours(args):
         f8 = {}
         for name in [n for n in [w.name] + OTHER if WORKLOADS[n].d == 128]:
             fw = WORKLOADS[name]
-            ms = statistics.median(time_fp8_forward(fw, 10, 3, flush))
-            bms = statistics.median(time_fp8_backward(fw, 10, 3, flush))
-            bf = time_workload(fw, 10, 3, flush)
+            ms = statistics.median(time_fp8_forward(fw, EXTRA_REPS, EXTRA_WARMUP, flush))
+            bms = statistics.median(time_fp8_backward(fw, EXTRA_REPS, EXTRA_WARMUP, flush))
+            bf = time_workload(fw, EXTRA_REPS, EXTRA_WARMUP, flush)
             f8[name] = {"fp8_fwd_ms": round(ms, 4),
                         "fp8_fwd_tflops": round(fw.fwd_flops() / ms / 1e9, 1),
                         "fp8_fwd_frac_of_fp8_peak": round(fw.fwd_flops() / ms / 1e9
@@ -716,7 +726,7 @@ def run_ours(args):
         alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
         ssd_res = {}
         for name, sw in SSD_WORKLOADS.items():
-            f_ms, b_ms = time_ssd(sw, 10, 3, flush)
+            f_ms, b_ms = time_ssd(sw, EXTRA_REPS, EXTRA_WARMUP, flush)
             fm, bm = statistics.median(f_ms), statistics.median(b_ms)
             ssd_res[name] = {
                 "fwd_ms": round(fm, 4), "bwd_ms": round(bm, 4),
@@ -731,7 +741,7 @@ def run_ours(args):
         # FLOPs are those of the visible pairs: N*W - W^2/2 per head under the
         # window, the sum of n^2/2 over documents of lengths n.
         for name, sw in EXTRA_WORKLOADS.items():
-            rw = time_workload(sw, 10, 3, flush)
+            rw = time_workload(sw, EXTRA_REPS, EXTRA_WARMUP, flush)
             extra[name] = {
                 "window": sw.window,
                 "documents": len(sw.doc_lengths),
