@@ -61,10 +61,14 @@ HEADLINE = "b4h16n8192d128"
 OTHER = ["b2h16n2048d64_causal", "b1h32n4096d128_causal", "b1h16n16384d128_causal"]
 METRIC = "attention backward TFLOP/s (bf16, 1xGB300) and fraction of dense bf16 peak"
 FLUSH_BYTES = 512 << 20
-# The extra workloads' timing: 10 warm-ups, then the median of 50 steps (200
-# on the small d = 64 workloads, whose steps take tens of microseconds).
-EXTRA_WARMUP = 10
-EXTRA_REPS = 50
+# The extra workloads' timing: the median of a short run (10 steps after 3
+# warm-ups; 200 steps on the d = 64 workloads, whose steps take tens of
+# microseconds), so that they run at full clock and compare with the burst
+# peak.  The headline's seconds-long loop gives the sustained figure: 50-step
+# runs of the larger workloads already settle under the power cap (the
+# N = 16384 causal main kernel at 1,362 TFLOP/s against 1,425-1,445).
+EXTRA_WARMUP = 3
+EXTRA_REPS = 10
 SMALL_REPS = 200
 
 
